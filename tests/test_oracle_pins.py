@@ -1,0 +1,289 @@
+"""Pins that tie the float64 oracle to facts other than itself.
+
+Each test checks the oracle against something it cannot share a mistake with: a closed form,
+a hand-derived example, brute-force pure-Python loops, torch's float64 cross-entropy (a library
+special case), central finite differences, the two-class logistic special case, or an
+invariant of the mathematics. Together they are chosen so that a dropped term, a wrong sign or
+index, a transposed operand, a wrong 'mean' denominator or a missing max-subtraction in the
+oracle fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+
+RNG = np.random.default_rng(12345)
+
+
+def _rand_case(T, H, V, x_std=1.0, w_std=0.5, seed=0):
+    r = np.random.default_rng(seed)
+    x = r.standard_normal((T, H)) * x_std
+    w = r.standard_normal((V, H)) * w_std
+    y = r.integers(0, V, size=T)
+    return x, w, y
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_zero_weight_closed_form(reduction):
+    """weight = 0: every logit is 0, so lse = ln V, l_t = ln V and dz = (1/V - onehot) g."""
+    T, H, V = 7, 5, 11
+    x, _, y = _rand_case(T, H, V, seed=1)
+    w = np.zeros((V, H))
+    out = oracle.flce(x, w, y, reduction, grad_loss=1.7)
+    lnV = math.log(V)
+    assert np.allclose(out["lse"], lnV, rtol=0, atol=1e-14)
+    expect_loss = T * lnV if reduction == "sum" else lnV
+    assert abs(out["loss"] - expect_loss) < 1e-12
+    g = 1.7 if reduction == "sum" else 1.7 / T
+    assert np.abs(out["grad_x"]).max() == 0.0
+    expect_gw = np.tile(g * x.sum(0) / V, (V, 1))
+    for t in range(T):
+        expect_gw[y[t]] -= g * x[t]
+    assert np.allclose(out["grad_weight"], expect_gw, rtol=0, atol=1e-13)
+
+
+def test_zero_x_closed_form():
+    """x = 0: logits vanish; grad_weight = 0 and grad_x[t] = g (mean_v W[v] - W[y_t])."""
+    T, H, V = 6, 4, 9
+    _, w, y = _rand_case(T, H, V, seed=2)
+    x = np.zeros((T, H))
+    out = oracle.flce(x, w, y, "mean")
+    assert abs(out["loss"] - math.log(V)) < 1e-14
+    assert np.abs(out["grad_weight"]).max() == 0.0
+    g = 1.0 / T
+    expect = g * (w.mean(0)[None, :] - w[y])
+    assert np.allclose(out["grad_x"], expect, rtol=0, atol=1e-15)
+
+
+def test_identical_rows_large_logits():
+    """All weight rows equal w: z[t, v] = x_t.w for every v, so lse = x_t.w + ln V exactly and
+    grad_x = 0. Logits near +-900 overflow exp() unless the row maximum is taken out first."""
+    T, H, V = 5, 3, 8
+    r = np.random.default_rng(3)
+    x = r.standard_normal((T, H)) * 300.0
+    wrow = np.array([1.0, -2.0, 0.5])
+    w = np.tile(wrow, (V, 1))
+    y = r.integers(0, V, size=T)
+    out = oracle.flce(x, w, y, "sum")
+    zt = x @ wrow
+    assert np.all(np.abs(zt) > 50)  # far outside exp()'s comfortable range somewhere
+    assert np.allclose(out["lse"], zt + math.log(V), rtol=1e-15, atol=1e-11)
+    assert abs(out["loss"] - T * math.log(V)) < 1e-9
+    assert np.allclose(out["grad_x"], 0.0, atol=1e-12)
+
+
+def test_hand_derived_2x2x3():
+    """x = [[1,0],[0,2]], W = [[1,0],[0,1],[1,1]], targets [2, 0], reduction mean.
+
+    z = [[1,0,1],[0,2,2]] so lse = [ln(1+2e), ln(1+2e^2)], l = [ln(1+2e)-1, ln(1+2e^2)],
+    p0 = [e,1,e]/(1+2e), p1 = [1,e^2,e^2]/(1+2e^2), dz_t = (p_t - onehot)/2,
+    grad_x[t] = [dz_t0 + dz_t2, dz_t1 + dz_t2], grad_W[v] = [dz_0v, 2 dz_1v].
+    """
+    e = math.e
+    x = np.array([[1.0, 0.0], [0.0, 2.0]])
+    w = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]])
+    y = np.array([2, 0])
+    out = oracle.flce(x, w, y, "mean")
+    lse = [math.log(1 + 2 * e), math.log(1 + 2 * e * e)]
+    loss = (lse[0] - 1 + lse[1]) / 2
+    p0 = np.array([e, 1, e]) / (1 + 2 * e)
+    p1 = np.array([1, e * e, e * e]) / (1 + 2 * e * e)
+    dz0 = (p0 - np.array([0, 0, 1])) / 2
+    dz1 = (p1 - np.array([1, 0, 0])) / 2
+    gx = np.array([[dz0[0] + dz0[2], dz0[1] + dz0[2]], [dz1[0] + dz1[2], dz1[1] + dz1[2]]])
+    gw = np.stack([np.array([dz0[v], 2 * dz1[v]]) for v in range(3)])
+    assert np.allclose(out["lse"], lse, rtol=0, atol=1e-15)
+    assert abs(out["loss"] - loss) < 1e-15
+    assert np.allclose(out["grad_x"], gx, rtol=0, atol=1e-15)
+    assert np.allclose(out["grad_weight"], gw, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_two_class_logistic(reduction):
+    """V = 2 is binary logistic regression: l_t = log(1 + exp(z_other - z_target)) and
+    d l_t / d z_target = -sigmoid(z_other - z_target)."""
+    T, H = 9, 4
+    r = np.random.default_rng(4)
+    x = r.standard_normal((T, H))
+    w = r.standard_normal((2, H))
+    y = r.integers(0, 2, size=T)
+    out = oracle.flce(x, w, y, reduction, grad_loss=0.8)
+    zt = np.einsum("th,th->t", x, w[y])
+    zo = np.einsum("th,th->t", x, w[1 - y])
+    margin = zo - zt
+    per_tok = np.log1p(np.exp(margin))
+    expect = per_tok.sum() if reduction == "sum" else per_tok.mean()
+    assert abs(out["loss"] - expect) < 1e-13
+    g = 0.8 if reduction == "sum" else 0.8 / T
+    sig = 1.0 / (1.0 + np.exp(-margin))
+    # dl/dz_other = sig, dl/dz_target = -sig; grad_x = g*sig*(w_other - w_target)
+    gx = g * sig[:, None] * (w[1 - y] - w[y])
+    assert np.allclose(out["grad_x"], gx, rtol=0, atol=1e-14)
+
+
+# ---------------------------------------------------------------- brute force and library
+
+def _brute_force(x, w, y, reduction, grad_loss):
+    """Pure-Python loops: logits, textbook log-softmax, and the chain rule by hand."""
+    T, H = len(x), len(x[0])
+    V = len(w)
+    z = [[sum(x[t][h] * w[v][h] for h in range(H)) for v in range(V)] for t in range(T)]
+    lse, per_tok = [], []
+    for t in range(T):
+        m = max(z[t])
+        s = math.fsum(math.exp(z[t][v] - m) for v in range(V))
+        lse.append(m + math.log(s))
+        per_tok.append(lse[t] - z[t][y[t]])
+    loss = math.fsum(per_tok) if reduction == "sum" else math.fsum(per_tok) / T
+    g = grad_loss if reduction == "sum" else grad_loss / T
+    dz = [[(math.exp(z[t][v] - lse[t]) - (1.0 if v == y[t] else 0.0)) * g for v in range(V)]
+          for t in range(T)]
+    gx = [[math.fsum(dz[t][v] * w[v][h] for v in range(V)) for h in range(H)] for t in range(T)]
+    gw = [[math.fsum(dz[t][v] * x[t][h] for t in range(T)) for h in range(H)] for v in range(V)]
+    return loss, lse, gx, gw
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 2), (3, 5, 7), (8, 16, 32), (5, 2, 31)])
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_brute_force_tiny(shape, reduction):
+    T, H, V = shape
+    x, w, y = _rand_case(T, H, V, seed=T * 100 + H * 10 + V)
+    out = oracle.flce(x, w, y, reduction, grad_loss=1.3, chunk=3)
+    loss, lse, gx, gw = _brute_force(x.tolist(), w.tolist(), y.tolist(), reduction, 1.3)
+    assert abs(out["loss"] - loss) <= 1e-12 * max(1.0, abs(loss))
+    assert np.allclose(out["lse"], lse, rtol=1e-13, atol=1e-13)
+    assert np.allclose(out["grad_x"], gx, rtol=1e-12, atol=1e-14)
+    assert np.allclose(out["grad_weight"], gw, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_against_torch_float64_cross_entropy(reduction):
+    """Library special case: materialised float64 logits + torch.nn.functional.cross_entropy,
+    gradients by autograd. T exceeds the oracle chunk so grad_weight accumulation is exercised."""
+    torch = pytest.importorskip("torch")
+    T, H, V = 37, 19, 53
+    x, w, y = _rand_case(T, H, V, seed=5)
+    out = oracle.flce(x, w, y, reduction, grad_loss=0.9, chunk=8)
+    xt = torch.tensor(x, dtype=torch.float64, requires_grad=True)
+    wt = torch.tensor(w, dtype=torch.float64, requires_grad=True)
+    yt = torch.tensor(y, dtype=torch.int64)
+    loss = torch.nn.functional.cross_entropy(xt @ wt.T, yt, reduction=reduction)
+    (loss * 0.9).backward()
+    assert abs(out["loss"] - loss.item()) < 1e-12 * max(1.0, abs(loss.item()))
+    assert np.allclose(out["grad_x"], xt.grad.numpy(), rtol=1e-11, atol=1e-14)
+    assert np.allclose(out["grad_weight"], wt.grad.numpy(), rtol=1e-11, atol=1e-14)
+    lse_t = torch.logsumexp(xt.detach() @ wt.detach().T, dim=1).numpy()
+    assert np.allclose(out["lse"], lse_t, rtol=1e-14, atol=1e-13)
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean"])
+def test_central_finite_differences(reduction):
+    T, H, V = 4, 3, 6
+    x, w, y = _rand_case(T, H, V, seed=6)
+    out = oracle.flce(x, w, y, reduction, grad_loss=1.0)
+    eps = 1e-6
+
+    def L(xx, ww):
+        return oracle.forward(xx, ww, y, reduction)[0]
+
+    fd_x = np.zeros_like(x)
+    for i in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[i] += eps
+        xm[i] -= eps
+        fd_x[i] = (L(xp, w) - L(xm, w)) / (2 * eps)
+    fd_w = np.zeros_like(w)
+    for i in np.ndindex(w.shape):
+        wp, wm = w.copy(), w.copy()
+        wp[i] += eps
+        wm[i] -= eps
+        fd_w[i] = (L(x, wp) - L(x, wm)) / (2 * eps)
+    assert np.allclose(out["grad_x"], fd_x, rtol=1e-6, atol=1e-8)
+    assert np.allclose(out["grad_weight"], fd_w, rtol=1e-6, atol=1e-8)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_dz_rows_sum_to_zero_and_weight_grad_columns_vanish():
+    T, H, V = 20, 8, 50
+    x, w, y = _rand_case(T, H, V, seed=7)
+    z = oracle.logits(x, w)
+    lse = oracle.log_sum_exp(z)
+    dz = oracle.dlogits(z, lse, y, 0.37)
+    assert np.abs(dz.sum(1)).max() < 1e-15
+    out = oracle.flce(x, w, y, "mean")
+    assert np.abs(out["grad_weight"].sum(0)).max() < 1e-15
+
+
+def test_shift_invariance():
+    """Adding the same vector a to every weight row shifts each logit row by x_t.a: the loss,
+    grad_x and grad_weight are unchanged and lse moves by x.a."""
+    T, H, V = 10, 6, 15
+    x, w, y = _rand_case(T, H, V, seed=8)
+    a = np.random.default_rng(9).standard_normal(H)
+    o1 = oracle.flce(x, w, y, "mean")
+    o2 = oracle.flce(x, w + a[None, :], y, "mean")
+    assert abs(o1["loss"] - o2["loss"]) < 1e-13
+    assert np.allclose(o2["lse"], o1["lse"] + x @ a, rtol=0, atol=1e-13)
+    assert np.allclose(o1["grad_x"], o2["grad_x"], rtol=0, atol=1e-14)
+    assert np.allclose(o1["grad_weight"], o2["grad_weight"], rtol=0, atol=1e-14)
+
+
+def test_sum_is_T_times_mean_and_grad_loss_is_linear():
+    T, H, V = 13, 7, 17
+    x, w, y = _rand_case(T, H, V, seed=10)
+    s = oracle.flce(x, w, y, "sum", grad_loss=1.0)
+    m = oracle.flce(x, w, y, "mean", grad_loss=1.0)
+    assert abs(s["loss"] - T * m["loss"]) < 1e-12
+    assert np.allclose(s["grad_x"], T * m["grad_x"], rtol=1e-13, atol=0)
+    assert np.allclose(s["grad_weight"], T * m["grad_weight"], rtol=1e-13, atol=0)
+    s2 = oracle.flce(x, w, y, "sum", grad_loss=-2.5)
+    assert np.allclose(s2["grad_x"], -2.5 * s["grad_x"], rtol=1e-14, atol=0)
+
+
+def test_chunk_size_does_not_change_result():
+    T, H, V = 33, 5, 21
+    x, w, y = _rand_case(T, H, V, seed=11)
+    a = oracle.flce(x, w, y, "mean", chunk=1)
+    b = oracle.flce(x, w, y, "mean", chunk=1000)
+    assert abs(a["loss"] - b["loss"]) < 1e-14
+    assert np.allclose(a["grad_weight"], b["grad_weight"], rtol=1e-13, atol=1e-16)
+    assert np.allclose(a["grad_x"], b["grad_x"], rtol=1e-13, atol=1e-16)
+
+
+def test_sampled_rows_match_full_run():
+    T, H, V = 40, 6, 25
+    x, w, y = _rand_case(T, H, V, seed=12)
+    full = oracle.flce(x, w, y, "mean", grad_loss=1.1)
+    rows = np.array([0, 7, 39, 13])
+    s = oracle.sampled_rows(x, w, y, rows, "mean", grad_loss=1.1)
+    assert np.allclose(s["lse"], full["lse"][rows], rtol=0, atol=1e-14)
+    assert np.allclose(s["grad_x"], full["grad_x"][rows], rtol=0, atol=1e-15)
+    z = x[rows] @ w.T
+    assert np.allclose(s["per_token_loss"], full["lse"][rows] - z[np.arange(4), y[rows]])
+
+
+def test_out_of_range_target_rejected():
+    x, w, y = _rand_case(3, 2, 4, seed=13)
+    y = y.copy()
+    y[1] = 4
+    with pytest.raises(ValueError):
+        oracle.forward(x, w, y)
+    y[1] = -1
+    with pytest.raises(ValueError):
+        oracle.forward(x, w, y)
+
+
+def test_statistical_band_tiny_workload():
+    """With x ~ N(0,1), W ~ N(0, 0.02^2) and targets independent of both, each logit is
+    N(0, 0.0004 H), so E[loss] = E[lse] ~= ln V + 0.0002 H (second-order expansion).
+    A sanity band (1%), not a pin on its own."""
+    from lm_head_linear_02_gb300.inputs import make_inputs
+    inp = make_inputs("tiny")
+    loss, _ = oracle.forward(inp.x, inp.weight, inp.target, "mean")
+    expect = math.log(inp.workload.V) + 0.0002 * inp.workload.H
+    assert abs(loss - expect) / expect < 0.01
