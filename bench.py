@@ -1,0 +1,405 @@
+"""Benchmark of the fused linear cross-entropy hot path (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = flce_forward + flce_backward (every kernel of the path) over one batch of the
+workload's synthetic inputs, already resident in HBM. Prints ONE JSON line on rank 0.
+
+* value: whole-job tokens/s (all ranks), from CUDA events over exactly K timed steps bracketed
+  by a barrier and a device synchronise on both sides, max over ranks.
+* roofline: the dominant tensor-core kernel role (largest summed launch time in the timed
+  region), timed per launch with CUDA events on its launch stream through libflce's timing
+  hooks; achieved = its algorithmic FLOPs / its launch time, against the measured dense-bf16
+  peak (sustained figure: the kernel runs inside a long step).
+* e2e: the same metric with host-resident inputs: each step copies x, weight and target from
+  pinned host memory, runs the path, and reads the loss back, all inside the timed region.
+* cpu_baseline: the float64 oracle timed on this host's cores on a bounded token sample.
+* --impl reference: the reference arm is the float64 oracle (there is no other implementation
+  to run): each step is a bounded token sample of the same workload, timed on the host cores.
+With N > 1 (torchrun) every rank runs an independent replica of the workload (weak scaling,
+no collective on the data path); the path has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from lm_head_linear_02_gb300 import roofline  # noqa: E402
+from lm_head_linear_02_gb300.inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "FLCE fwd+bwd tokens/s and % dense-BF16 tensor peak at T=16384,H=4096,V=128256"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "llama3_head_t16384"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CSRC = os.path.join(ROOT, "lm_head_linear_02_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_digest() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(role: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, or None if the kernels changed."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get("roles", {}).get(role)
+    if not entry or rec.get("sources_sha256") != sources_digest():
+        return None
+    if entry.get("workload") != workload:
+        return None
+    return entry.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 8:
+                continue
+            try:
+                sm.append(float(r[0]))
+                smax.append(float(r[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ reference arm
+
+def oracle_sample_step(inp, n_tokens: int, step: int):
+    """One oracle step on a token sample (different rows each step)."""
+    import oracle
+
+    T = inp.workload.T
+    start = (step * n_tokens) % max(1, T - n_tokens + 1)
+    sl = slice(start, start + n_tokens)
+    oracle.flce(inp.x[sl], inp.weight, inp.target[sl], "mean")
+
+
+def run_reference(args, wl, rank: int, world: int):
+    if rank != 0:
+        return
+    inp = make_inputs(wl)
+    n_tok = args.oracle_tokens
+    for s in range(args.warmup):
+        oracle_sample_step(inp, n_tok, s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        oracle_sample_step(inp, n_tok, args.warmup + s)
+    dt = time.perf_counter() - t0
+    value = n_tok * args.steps / dt
+    cores = os.cpu_count()
+    sample = (f"{n_tok} tokens per step of {wl.name} (full H={wl.H}, V={wl.V}), float64 numpy "
+              f"oracle forward+backward")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl, 0),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def workload_config(wl, n_slabs):
+    return {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "vocab": wl.V,
+            "dtype": wl.dtype, "targets": wl.target_dist, "reduction": "mean",
+            "backward_vocab_slabs": n_slabs,
+            "l2": "inputs larger than L2 (weight alone is %.2f GB > 129 MB)" % (
+                wl.V * wl.H * (2 if wl.dtype == "bf16" else 4) / 1e9),
+            "parallelism": "replicas"}
+
+
+# ------------------------------------------------------------------------------ our arm
+
+def cpu_baseline(inp, n_tokens: int):
+    import oracle
+
+    T = inp.workload.T
+    sl = slice(0, min(n_tokens, T))
+    t0 = time.perf_counter()
+    oracle.flce(inp.x[sl], inp.weight, inp.target[sl], "mean")
+    dt = time.perf_counter() - t0
+    n = sl.stop - sl.start
+    return {"value": n / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {n} tokens of {inp.workload.name} (full H, V), float64 numpy "
+                      f"oracle forward+backward, {dt:.1f} s"}
+
+
+def run_ours(args, wl, rank: int, world: int, dist):
+    import torch
+
+    from lm_head_linear_02_gb300 import autograd as A
+    from lm_head_linear_02_gb300 import binding as B
+    from lm_head_linear_02_gb300 import build as build_mod
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if not build_mod.up_to_date():
+        raise RuntimeError("libflce.so is missing or stale: run __graft_entry__.build() first")
+    B.lib()
+
+    t_gen = time.perf_counter()
+    inp = make_inputs(wl)
+    log(f"[rank {rank}] inputs generated in {time.perf_counter() - t_gen:.1f} s")
+    T, H, V = wl.T, wl.H, wl.V
+    dt_code = B.dtype_code(wl.dtype)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    if wl.dtype == "bf16":
+        hx = torch.from_numpy(inp.x_bits.view(np.int16)).view(torch.bfloat16)
+        hw = torch.from_numpy(inp.weight_bits.view(np.int16)).view(torch.bfloat16)
+    else:
+        hx = torch.from_numpy(inp.x)
+        hw = torch.from_numpy(inp.weight)
+    hy = torch.from_numpy(inp.target)
+    hx, hw, hy = hx.pin_memory(), hw.pin_memory(), hy.pin_memory()
+    x = hx.to(dev)
+    w = hw.to(dev)
+    y = hy.to(dev)
+    red = B.FLCE_REDUCTION_MEAN
+    fwd_ws = B.flce_forward_workspace_size(T, H, V, dt_code)
+    bwd_ws = B.flce_backward_workspace_size(T, H, V, dt_code)
+    vc = B.flce_backward_slab_width(T, H, V, dt_code)
+    n_slabs = math.ceil(V / vc)
+    ws = torch.empty(max(fwd_ws, bwd_ws), dtype=torch.uint8, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    gl = torch.ones(1, dtype=torch.float32, device=dev)
+    gx = torch.empty_like(x)
+    gw = torch.empty_like(w)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step():
+        B.flce_forward(x.data_ptr(), w.data_ptr(), y.data_ptr(), T, H, V, dt_code, red,
+                       loss.data_ptr(), lse.data_ptr(), ws.data_ptr(), fwd_ws, status.data_ptr(),
+                       sp)
+        B.flce_backward(x.data_ptr(), w.data_ptr(), y.data_ptr(), lse.data_ptr(), T, H, V,
+                        dt_code, red, gl.data_ptr(), gx.data_ptr(), gw.data_ptr(), ws.data_ptr(),
+                        bwd_ws, status.data_ptr(), sp)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    # warm-up
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    A.check_status(status)
+
+    # ---- timed region (device-resident inputs)
+    B.flce_timing_read()  # discard warm-up records
+    B.flce_timing_enable(True)
+    torch.cuda.reset_peak_memory_stats(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for k in range(args.steps):
+        B.flce_forward(x.data_ptr(), w.data_ptr(), y.data_ptr(), T, H, V, dt_code, red,
+                       loss.data_ptr(), lse.data_ptr(), ws.data_ptr(), fwd_ws, status.data_ptr(),
+                       sp)
+        ev[2 * k + 1].record(stream)
+        B.flce_backward(x.data_ptr(), w.data_ptr(), y.data_ptr(), lse.data_ptr(), T, H, V,
+                        dt_code, red, gl.data_ptr(), gx.data_ptr(), gw.data_ptr(), ws.data_ptr(),
+                        bwd_ws, status.data_ptr(), sp)
+        ev[2 * k + 2].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    B.flce_timing_enable(False)
+    per_role = B.flce_timing_read()
+    A.check_status(status)
+    total_ms = ev[0].elapsed_time(ev[-1])
+    fwd_ms = [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(args.steps)]
+    bwd_ms = [ev[2 * k + 1].elapsed_time(ev[2 * k + 2]) for k in range(args.steps)]
+    peak_mem = torch.cuda.max_memory_allocated(dev)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = t.item()
+
+    # ---- end-to-end: host-resident inputs, H2D copies + D2H loss read inside the timed region
+    e2e_steps = max(1, min(args.steps, 5))
+    h_loss = torch.empty(1, dtype=torch.float32).pin_memory()
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        x.copy_(hx, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        y.copy_(hy, non_blocking=True)
+        step()
+        h_loss.copy_(loss, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        _ = float(h_loss[0])
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = t.item()
+    A.check_status(status)
+    if rank != 0:
+        return
+
+    # ---- roofline of the dominant kernel role
+    peaks, peak_kind = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    role_flops = {r: args.steps * roofline.flops(T, H, V, "fwd") for r in B.TIMING_ROLES}
+    dom = max(per_role, key=lambda r: per_role[r][1])
+    n_launch, ms_sum = per_role[dom]
+    achieved = role_flops[dom] / (ms_sum * 1e-3) / 1e12
+    traffic = recorded_traffic(dom, wl.name)
+    ms_step = total_ms / args.steps
+    step_tflops = roofline.flops(T, H, V, "fwd_bwd") / (ms_step * 1e-3) / 1e12
+    # forward: projection kernel + combine + finalize; backward: dz, grad_W, grad_x per slab;
+    # the fp32 path adds the TF32 operand splits (2 in the forward, 4 in the backward).
+    launches_per_step = 3 + 3 * n_slabs + (6 if wl.dtype == "f32" else 0)
+    cpu = cpu_baseline(inp, args.oracle_tokens) if world == 1 else None
+    out = {
+        "metric": METRIC, "value": world * T * args.steps / (total_ms * 1e-3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+        "data": "synthetic: seeded PCG64, x~N(0,1), weight~N(0,0.02^2), targets %s" % wl.target_dist,
+        "config": workload_config(wl, n_slabs),
+        "fwd_ms": statistics.median(fwd_ms), "bwd_ms": statistics.median(bwd_ms),
+        "fwd_tokens_per_s": T / (statistics.median(fwd_ms) * 1e-3),
+        "tensor_tflops_step": step_tflops,
+        "tensor_frac_of_measured": {"burst": step_tflops / peak_burst,
+                                     "sustained": step_tflops / peak_sus,
+                                     "peaks_source": peak_kind},
+        "flops_per_step": roofline.flops(T, H, V, "fwd_bwd"),
+        "roles_ms_per_step": {r: per_role[r][1] / args.steps for r in per_role},
+        "roofline": {"bound": "tensor", "kernel": f"k_umma_gemm ({dom})",
+                     "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s",
+                     "frac": achieved / peak_sus, "traffic": traffic,
+                     "launches": n_launch, "peak_source": f"bf16_tflops_sustained of {peak_kind}"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * T * e2e_steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": int(hx.numel() * hx.element_size() +
+                                          hw.numel() * hw.element_size() + hy.numel() * 8),
+                "d2h_bytes_per_step": 4},
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+        "peak_mem_gb": peak_mem / 1e9,
+        "workspace_gb": max(fwd_ws, bwd_ws) / 1e9,
+        "logits_bf16_gb": 2 * T * V / 1e9,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--oracle-tokens", type=int, default=64,
+                    help="token sample per oracle step (CPU baseline / reference arm)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        if args.impl == "reference":
+            run_reference(args, wl, rank, world)
+        else:
+            run_ours(args, wl, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

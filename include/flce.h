@@ -1,0 +1,150 @@
+/*
+ * flce.h - C ABI of libflce, a fused linear cross-entropy (FLCE) for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation. "Fused linear + cross-entropy" (KernelIndex operation page), summary and
+ * "Semantics" table: x float[tokens, hidden], weight float[vocab, hidden], target int64[tokens],
+ * loss float[1]; the LM-head projection z = x . weight^T is scored by cross-entropy against the
+ * integer targets without ever materialising the tokens x vocab logits. "[example]
+ * fused_linear_cross_entropy kernel" (Helion PR #1268), description: the forward computes the
+ * per-token log-sum-exp (kept for the backward) and the target logits; the backward recomputes
+ * the logits to form grad_input and grad_weight. "feat(FLCE): add helion version of fused linear
+ * cross entropy" (Liger-Kernel PR #928), failing-test list: reductions 'sum' and 'mean'.
+ *
+ *   lse[t]  = ln sum_v exp(z[t, v])                     z = x . weight^T
+ *   loss    = sum_t (lse[t] - z[t, target[t]])          (SUM),  divided by T for MEAN
+ *   dz      = (softmax(z) - onehot(target)) * g         g = grad_loss (SUM) or grad_loss / T (MEAN)
+ *   grad_x  = dz . weight                               grad_weight = dz^T . x
+ *
+ * Layout. Every matrix is row-major with its last index contiguous: x[T][H], weight[V][H],
+ * grad_x[T][H], grad_weight[V][H]. target is int64[T]; lse is float32[T]; loss and grad_loss are
+ * float32[1]. All pointers except those documented as host pointers are DEVICE pointers on the
+ * current CUDA device. Matrix rows must start on 16-byte boundaries: H * element size must be a
+ * multiple of 16 bytes and every base pointer 16-byte aligned, else FLCE_ERR_UNSUPPORTED.
+ *
+ * Types. FLCE_DTYPE_BF16: x, weight, grad_x, grad_weight are bfloat16; products are summed in
+ * fp32 on the tensor cores and the softmax is evaluated in fp32. FLCE_DTYPE_F32: those four are
+ * float32 and every contraction runs as three TF32 tensor-core products (hi*hi + hi*lo + lo*hi)
+ * with fp32 accumulation. lse, loss and grad_loss are float32 in both cases.
+ *
+ * Ownership. The caller owns every buffer, including the workspace and the device status word;
+ * the library allocates no device memory. Inputs are never written ("No mutation or aliasing",
+ * KernelIndex "Semantics"): an output that overlaps an input or another output is rejected with
+ * FLCE_ERR_ALIAS.
+ *
+ * Asynchrony. Both compute calls only enqueue work on `stream` (a cudaStream_t; NULL means the
+ * legacy default stream) and return. Results are valid once the stream has been synchronised.
+ * A call that fails validation (FLCE_ERR_ARG, _UNSUPPORTED, _WORKSPACE, _ALIAS) has enqueued
+ * nothing; after FLCE_ERR_CUDA part of the work may have been enqueued and the outputs are
+ * undefined.
+ *
+ * Errors. Host-detectable problems are returned as negative codes (see FLCE_ERR_*). Problems only
+ * the device can see are OR-ed into the device int *status as FLCE_STATUS_* bits and never trap:
+ * a target outside [0, V) makes the loss NaN; a pipeline wait that exceeds its time limit makes
+ * the kernel stop early and leaves its outputs undefined. The caller zeroes *status before the
+ * first call and reads it after synchronising.
+ *
+ * Determinism. Results are bitwise identical from run to run on the same device for the same
+ * inputs: there are no floating-point atomics and every reduction has a fixed order.
+ */
+#ifndef FLCE_H
+#define FLCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define FLCE_OK 0
+#define FLCE_ERR_ARG (-1)         /* null pointer, T/H/V <= 0 or too large, unknown enum value   */
+#define FLCE_ERR_UNSUPPORTED (-2) /* misaligned pointer or row stride, or not an sm_103 device   */
+#define FLCE_ERR_WORKSPACE (-3)   /* workspace pointer null or smaller than the size query says  */
+#define FLCE_ERR_ALIAS (-4)       /* an output overlaps an input or another output               */
+#define FLCE_ERR_CUDA (-5)        /* a CUDA runtime/driver call failed (launch, tensor map, ...)  */
+
+/* Device status bits (OR-ed into *status by the kernels). */
+#define FLCE_STATUS_TARGET_RANGE 1 /* some target[t] outside [0, V): the loss is NaN             */
+#define FLCE_STATUS_TIMEOUT 2      /* a pipeline wait ran out of time; outputs are undefined      */
+
+/* Element type of x, weight, grad_x and grad_weight. */
+#define FLCE_DTYPE_BF16 0
+#define FLCE_DTYPE_F32 1
+
+/* Reduction over tokens ("sum" and "mean", Liger-Kernel PR #928 failing-test list). */
+#define FLCE_REDUCTION_SUM 0
+#define FLCE_REDUCTION_MEAN 1
+
+/* Bytes of device workspace flce_forward needs for this problem; 0 for invalid arguments.
+ * Holds per-(vocab tile, token) partial log-sum-exp terms, the target logits and per-block loss
+ * sums (plus the TF32 hi/lo operand copies for FLCE_DTYPE_F32). Pure host arithmetic. */
+size_t flce_forward_workspace_size(int64_t T, int64_t H, int64_t V, int dtype);
+
+/* Bytes of device workspace flce_backward needs; 0 for invalid arguments. Holds one bounded
+ * vocab slab of dz (T x Vc, never the full T x V logits) and, for bf16, the fp32 grad_x
+ * accumulator (T x H). Pure host arithmetic. */
+size_t flce_backward_workspace_size(int64_t T, int64_t H, int64_t V, int dtype);
+
+/* Vocab slab width Vc the backward uses for this problem (a multiple of 256), 0 if invalid. */
+int64_t flce_backward_slab_width(int64_t T, int64_t H, int64_t V, int dtype);
+
+/* Process-wide override of the backward vocab slab width: vc = 0 restores the automatic choice
+ * (a dz slab of at most 512 MiB), otherwise vc must be a positive multiple of 256. Affects the
+ * size query and the backward alike, so set it before querying the workspace size. A tuning and
+ * testing knob: it trades workspace memory against the number of slab passes. Returns FLCE_OK
+ * or FLCE_ERR_ARG. */
+int flce_set_backward_slab_width(int64_t vc);
+
+/*
+ * Forward ("[example] fused_linear_cross_entropy kernel", Helion PR #1268, description of the
+ * forward pass): computes loss[0] and the per-token log-sum-exp lse[T] that flce_backward needs.
+ *   x [T][H], weight [V][H]  (dtype), target [T] int64   - inputs, device, read only
+ *   loss [1] float32, lse [T] float32                     - outputs, device
+ *   workspace: device, >= flce_forward_workspace_size() bytes, 256-byte aligned, scratch only
+ *   status: device int, OR-ed with FLCE_STATUS_* bits
+ *   stream: cudaStream_t to enqueue on
+ * Returns FLCE_OK or a negative FLCE_ERR_* code.
+ */
+int flce_forward(const void* x, const void* weight, const int64_t* target,
+                 int64_t T, int64_t H, int64_t V, int dtype, int reduction,
+                 float* loss, float* lse,
+                 void* workspace, size_t workspace_bytes, int* status, void* stream);
+
+/*
+ * Backward ("[example] fused_linear_cross_entropy kernel", Helion PR #1268, description of the
+ * backward pass; the atomic grad_weight accumulation there is replaced by a deterministic
+ * vocab-slab schedule): recomputes the logits slab by slab, forms dz in registers and writes
+ *   grad_x [T][H] = dz . weight   and   grad_weight [V][H] = dz^T . x     (dtype, device)
+ * x, weight, target, lse: as passed to / produced by flce_forward (device, read only)
+ * grad_loss [1] float32: device, the upstream gradient of loss
+ * workspace: device, >= flce_backward_workspace_size() bytes, 256-byte aligned, scratch only
+ * Returns FLCE_OK or a negative FLCE_ERR_* code.
+ */
+int flce_backward(const void* x, const void* weight, const int64_t* target, const float* lse,
+                  int64_t T, int64_t H, int64_t V, int dtype, int reduction,
+                  const float* grad_loss, void* grad_x, void* grad_weight,
+                  void* workspace, size_t workspace_bytes, int* status, void* stream);
+
+/* Per-launch timing of the contraction kernels, for benchmarks. While enabled (on != 0), each
+ * tensor-core kernel launch is bracketed by two CUDA events recorded on its launch stream (the
+ * library creates the events; it allocates no device memory). flce_timing_read() waits for the
+ * recorded events and returns, per kernel role, the number of launches and their summed
+ * duration in milliseconds since the previous read, then forgets them. Roles (arrays of 4):
+ *   0 forward projection + online log-sum-exp, 1 backward dz, 2 backward grad_weight,
+ *   3 backward grad_x.
+ * Process-wide and not thread-safe. Returns FLCE_OK, FLCE_ERR_ARG or FLCE_ERR_CUDA. */
+int flce_timing_enable(int on);
+int flce_timing_read(int64_t counts[4], double ms[4]);
+
+/* Static, human-readable name of a return code. Never NULL. */
+const char* flce_strerror(int code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int flce_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H */

@@ -1,0 +1,289 @@
+// epilogues.cuh - what each FLCE kernel does with a finished 128 x 256 fp32 accumulator tile.
+//
+// Every epilogue thread owns one accumulator row (one TMEM lane) and walks its 256 columns in
+// eight 32-column chunks (tcgen05.ld 32x32b.x32), so the per-row reductions of the softmax are
+// plain in-thread loops with no cross-thread traffic.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "gemm.cuh"
+
+namespace flce {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void load_chunk(uint32_t taddr, int c, float (&v)[32]) {
+  __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp issues it together
+  uint32_t r[32];
+  tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
+  tmem_ld_wait(r);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Store 32 consecutive fp32 values as bf16 (64 bytes, 16-byte aligned destination), or only
+// the first `n` (a multiple of 8) of them.
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&v)[32], int n) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (q * 8 < n) {
+      uint4 w;
+      w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+      w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+      w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+      w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+      d[q] = w;
+    }
+  }
+}
+
+// Store up to 32 fp32 values (n a multiple of 4, destination 16-byte aligned).
+__device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32], int n) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    if (q * 4 < n) d[q] = make_float4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
+}
+
+// TF32 split of an fp32 value: hi keeps the top 10 mantissa bits (rounded to nearest), and
+// lo = x - hi is exact in fp32. hi + lo == x.
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+  uint32_t h;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
+  hi = __uint_as_float(h);
+  lo = x - hi;
+}
+
+// ------------------------------------------------------------------------------- forward
+// "[example] fused_linear_cross_entropy kernel" (Helion PR #1268), forward: a tiled matmul
+// feeding an online softmax that yields the log-sum-exp and the target logit of each row.
+// Each (vocab tile, token) pair leaves a partial (max m, sum of exp(z - m)) that the combine
+// kernel merges in a fixed order; the one tile holding target[t] also writes z[t, target[t]].
+// Vocab columns >= V are masked to -inf.
+struct FwdEpi {
+  struct Args {
+    const int64_t* target;
+    float* part_m;  // [n_tiles][T]
+    float* part_s;  // [n_tiles][T]
+    float* zy;      // [T]
+    int T, V;
+  };
+  struct State {};
+  static __device__ __forceinline__ void init(const Args&, State&) {}
+
+  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
+                                              uint32_t taddr) {
+    const int t = mb * kBM + row;
+    const bool valid = t < a.T;
+    const int n0 = nb * kBN;
+    const long long y = valid ? static_cast<long long>(a.target[t]) : -1ll;
+    const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
+    float m = -INFINITY, s = 0.f, zy = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int c0 = n0 + c * 32;
+      if (c0 >= a.V) break;  // uniform across the warp
+      float v[32];
+      load_chunk(taddr, c, v);
+      if (c0 + 32 > a.V) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j >= a.V) v[j] = -INFINITY;
+      }
+      const int q = rel - c * 32;
+      if (q >= 0 && q < 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j == q) zy = v[j];
+      }
+      float cm0 = v[0], cm1 = v[1];
+#pragma unroll
+      for (int j = 2; j < 32; j += 2) {
+        cm0 = fmaxf(cm0, v[j]);
+        cm1 = fmaxf(cm1, v[j + 1]);
+      }
+      const float mn = fmaxf(m, fmaxf(cm0, cm1));
+      const float mnl = mn * kLog2e;
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        s0 += ex2(fmaf(v[j + 0], kLog2e, -mnl));
+        s1 += ex2(fmaf(v[j + 1], kLog2e, -mnl));
+        s2 += ex2(fmaf(v[j + 2], kLog2e, -mnl));
+        s3 += ex2(fmaf(v[j + 3], kLog2e, -mnl));
+      }
+      s = s * ex2((m - mn) * kLog2e) + ((s0 + s1) + (s2 + s3));
+      m = mn;
+    }
+    if (valid) {
+      const size_t o = static_cast<size_t>(nb) * a.T + t;
+      a.part_m[o] = m;
+      a.part_s[o] = s;
+      if (rel >= 0) a.zy[t] = zy;
+    }
+  }
+};
+
+// ------------------------------------------------------------------------------- backward dz
+// "[example] fused_linear_cross_entropy kernel" (Helion PR #1268), backward: the logits are
+// recomputed and turned into dz = (softmax - onehot(target)) * g in registers; here they are
+// written to a bounded vocab slab (T x Vc) that feeds the two gradient contractions.
+// Columns outside the slab are stored as 0; rows >= T are not stored.
+template <bool kTF32>
+struct DzEpi {
+  struct Args {
+    const int64_t* target;
+    const float* lse;
+    const float* grad_loss;
+    float scale;
+    void* dz;      // bf16 [T][ldz] or fp32 hi [T][ldz]
+    float* dz_lo;  // fp32 lo [T][ldz]          (tf32)
+    float* dzt_hi; // fp32 [slab_w][ldt]        (tf32)
+    float* dzt_lo; // fp32 [slab_w][ldt]        (tf32)
+    int ldz, ldt;
+    int T, slab0, slab_w;
+  };
+  struct State {
+    float g;
+  };
+  static __device__ __forceinline__ void init(const Args& a, State& st) {
+    st.g = __ldg(a.grad_loss) * a.scale;
+  }
+
+  static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
+                                              uint32_t taddr) {
+    const int t = mb * kBM + row;
+    const bool valid = t < a.T;
+    const float lsel = valid ? __ldg(a.lse + t) * kLog2e : 0.f;
+    const long long y = valid ? static_cast<long long>(__ldg(a.target + t)) : -1ll;
+    const int n0 = nb * kBN;  // slab-relative column of the tile
+    const long long rel = y - a.slab0 - n0;
+    const float g = st.g;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int c0 = n0 + c * 32;
+      if (c0 >= a.slab_w) break;  // uniform
+      float v[32];
+      load_chunk(taddr, c, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float d = ex2(fmaf(v[j], kLog2e, -lsel)) * g;
+        if (rel == c * 32 + j) d -= g;
+        if (c0 + j >= a.slab_w) d = 0.f;
+        v[j] = d;
+      }
+      if (!valid) continue;
+      if constexpr (!kTF32) {
+        store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.dz) + static_cast<size_t>(t) * a.ldz + c0,
+                      v, 32);
+      } else {
+        float hi[32], lo[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) split_tf32(v[j], hi[j], lo[j]);
+        store_f32x32(reinterpret_cast<float*>(a.dz) + static_cast<size_t>(t) * a.ldz + c0, hi, 32);
+        store_f32x32(a.dz_lo + static_cast<size_t>(t) * a.ldz + c0, lo, 32);
+        // Transposed copies: column c0 + j of this row goes to row c0 + j, column t. A warp's
+        // 32 lanes hold 32 consecutive t, so each of these stores is one coalesced 128 B line.
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (c0 + j < a.slab_w) {
+            a.dzt_hi[static_cast<size_t>(c0 + j) * a.ldt + t] = hi[j];
+            a.dzt_lo[static_cast<size_t>(c0 + j) * a.ldt + t] = lo[j];
+          }
+        }
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------------------- grad_weight
+// grad_weight[slab rows, :] = dz_slab^T . x : the contraction runs over all T tokens, so each
+// output tile is complete when it leaves TMEM and is written exactly once.
+template <bool kF32Out>
+struct GradWEpi {
+  struct Args {
+    void* grad_w;  // [V][H]
+    int H, slab0, slab_w;
+  };
+  struct State {};
+  static __device__ __forceinline__ void init(const Args&, State&) {}
+
+  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
+                                              uint32_t taddr) {
+    const int r = mb * kBM + row;  // slab-relative vocab row
+    const bool valid = r < a.slab_w;
+    const size_t vrow = static_cast<size_t>(a.slab0) + r;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int h0 = nb * kBN + c * 32;
+      if (h0 >= a.H) break;
+      float v[32];
+      load_chunk(taddr, c, v);
+      if (!valid) continue;
+      const int n = min(32, a.H - h0);
+      if constexpr (kF32Out)
+        store_f32x32(reinterpret_cast<float*>(a.grad_w) + vrow * a.H + h0, v, n);
+      else
+        store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.grad_w) + vrow * a.H + h0, v, n);
+    }
+  }
+};
+
+// ------------------------------------------------------------------------------- grad_x
+// grad_x = sum over vocab slabs of dz_slab . W_slab: a split-K over the vocabulary whose parts
+// are added in slab order into an fp32 accumulator (deterministic; no atomics).
+//   mode 0: only slab   -> out = D
+//   mode 1: first slab  -> acc = D
+//   mode 2: middle slab -> acc += D
+//   mode 3: last slab   -> out = acc + D
+// For fp32 outputs `acc` and `out` are the same buffer.
+template <bool kF32Out>
+struct GradXEpi {
+  struct Args {
+    float* acc;   // [T][H] fp32
+    void* out;    // [T][H] dtype
+    int T, H, mode;
+  };
+  struct State {};
+  static __device__ __forceinline__ void init(const Args&, State&) {}
+
+  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
+                                              uint32_t taddr) {
+    const int t = mb * kBM + row;
+    const bool valid = t < a.T;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int h0 = nb * kBN + c * 32;
+      if (h0 >= a.H) break;
+      float v[32];
+      load_chunk(taddr, c, v);
+      if (!valid) continue;
+      const int n = min(32, a.H - h0);
+      const size_t o = static_cast<size_t>(t) * a.H + h0;
+      if (a.mode >= 2) {
+        const float4* s = reinterpret_cast<const float4*>(a.acc + o);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (q * 4 < n) {
+            const float4 p = s[q];
+            v[q * 4 + 0] += p.x;
+            v[q * 4 + 1] += p.y;
+            v[q * 4 + 2] += p.z;
+            v[q * 4 + 3] += p.w;
+          }
+        }
+      }
+      if (a.mode == 1 || a.mode == 2 || kF32Out) {
+        store_f32x32((a.mode == 1 || a.mode == 2) ? a.acc + o : reinterpret_cast<float*>(a.out) + o,
+                     v, n);
+      } else {
+        store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.out) + o, v, n);
+      }
+    }
+  }
+};
+
+}  // namespace flce

@@ -1,0 +1,551 @@
+// flce_abi.cu - the C ABI of libflce: argument validation, workspace carve-up, TMA tensor-map
+// encoding and launch sequencing. All compute runs in the kernels of flce_fwd.cu / flce_bwd.cu;
+// this file only checks, plans and enqueues. Nothing here allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "flce_internal.h"
+
+namespace flce {
+
+// ------------------------------------------------------------------------------- device
+
+bool current_device(Device* d) {
+  static std::mutex mu;
+  static Device cache[64];
+  int id = -1;
+  if (cudaGetDevice(&id) != cudaSuccess || id < 0) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (id < 64 && cache[id].id == id) {
+    *d = cache[id];
+    return true;
+  }
+  Device x;
+  x.id = id;
+  if (cudaDeviceGetAttribute(&x.sms, cudaDevAttrMultiProcessorCount, id) != cudaSuccess ||
+      cudaDeviceGetAttribute(&x.cc_major, cudaDevAttrComputeCapabilityMajor, id) != cudaSuccess ||
+      cudaDeviceGetAttribute(&x.cc_minor, cudaDevAttrComputeCapabilityMinor, id) != cudaSuccess)
+    return false;
+  if (id < 64) cache[id] = x;
+  *d = x;
+  return true;
+}
+
+// ------------------------------------------------------------------------------- tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || (row_bytes & 15u) != 0) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  std::memset(tm, 0, sizeof(*tm));
+  return enc(tm, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------------------- timing
+// Optional event brackets around each contraction launch (see flce_timing_enable).
+
+namespace {
+struct TimedLaunch {
+  int role;
+  cudaEvent_t begin, end;
+};
+std::mutex g_timing_mu;
+bool g_timing_on = false;
+std::vector<TimedLaunch> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+}  // namespace
+
+// Runs `launch` (returning cudaError_t); brackets it with events when timing is enabled.
+template <class F>
+cudaError_t timed_launch(int role, cudaStream_t s, F&& launch) {
+  bool on;
+  {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    on = g_timing_on;
+  }
+  if (!on) return launch();
+  cudaEvent_t b, e;
+  {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    b = take_event();
+    e = take_event();
+  }
+  if (!b || !e) return cudaErrorMemoryAllocation;
+  cudaError_t r = cudaEventRecord(b, s);
+  if (r != cudaSuccess) return r;
+  r = launch();
+  if (r != cudaSuccess) return r;
+  r = cudaEventRecord(e, s);
+  if (r != cudaSuccess) return r;
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  g_pending.push_back(TimedLaunch{role, b, e});
+  return cudaSuccess;
+}
+
+}  // namespace flce
+
+// ================================================================================ C ABI
+
+namespace {
+
+using flce::kTileM;
+using flce::kTileN;
+
+constexpr int64_t kMaxDim = int64_t(1) << 24;          // T, V bound (tile counts fit in int)
+constexpr int64_t kMaxHidden = int64_t(1) << 20;
+constexpr size_t kAlign = 256;
+constexpr int64_t kSlabBudgetBytes = int64_t(512) << 20;  // dz slab (all its copies) per slab
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+inline size_t align_up(size_t a) { return (a + kAlign - 1) / kAlign * kAlign; }
+
+int elem_bytes(int dtype) { return dtype == FLCE_DTYPE_BF16 ? 2 : 4; }
+
+bool dims_ok(int64_t T, int64_t H, int64_t V, int dtype) {
+  if (dtype != FLCE_DTYPE_BF16 && dtype != FLCE_DTYPE_F32) return false;
+  if (T <= 0 || H <= 0 || V <= 0) return false;
+  if (T > kMaxDim || V > kMaxDim || H > kMaxHidden) return false;
+  if (cdiv(T, kTileM) * cdiv(V, kTileN) >= (int64_t(1) << 31)) return false;
+  return true;
+}
+
+// Sequential carve-up of a workspace into 256-byte aligned regions.
+struct Carver {
+  size_t off = 0;
+  uint8_t* base = nullptr;
+  void* take(size_t bytes) {
+    void* p = base ? base + off : nullptr;
+    off = align_up(off + bytes);
+    return p;
+  }
+};
+
+struct FwdWs {
+  float *part_m, *part_s, *zy, *block_sums;
+  float *x_hi, *x_lo, *w_hi, *w_lo;  // f32 path only
+};
+
+size_t carve_fwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, FwdWs* w) {
+  const int64_t nt = cdiv(V, kTileN);
+  FwdWs r{};
+  r.part_m = static_cast<float*>(c.take(sizeof(float) * nt * T));
+  r.part_s = static_cast<float*>(c.take(sizeof(float) * nt * T));
+  r.zy = static_cast<float*>(c.take(sizeof(float) * T));
+  r.block_sums = static_cast<float*>(c.take(sizeof(float) * cdiv(T, 256)));
+  if (dtype == FLCE_DTYPE_F32) {
+    r.x_hi = static_cast<float*>(c.take(sizeof(float) * T * H));
+    r.x_lo = static_cast<float*>(c.take(sizeof(float) * T * H));
+    r.w_hi = static_cast<float*>(c.take(sizeof(float) * V * H));
+    r.w_lo = static_cast<float*>(c.take(sizeof(float) * V * H));
+  }
+  if (w) *w = r;
+  return c.off;
+}
+
+std::atomic<int64_t> g_slab_override{0};
+
+int64_t slab_width(int64_t T, int64_t V, int dtype) {
+  const int64_t vmax = round_up(V, kTileN);
+  const int64_t forced = g_slab_override.load();
+  if (forced > 0) return forced < vmax ? forced : vmax;
+  // bf16: one bf16 slab. f32: hi/lo slabs in both [T][Vc] and [Vc][T] orientation.
+  const int64_t per_col = dtype == FLCE_DTYPE_BF16 ? 2 * T : 16 * round_up(T, 4);
+  int64_t vc = kSlabBudgetBytes / per_col / kTileN * kTileN;
+  if (vc < kTileN) vc = kTileN;
+  return vc < vmax ? vc : vmax;
+}
+
+struct BwdWs {
+  int64_t vc, n_slabs, ldT, ldV;
+  void* dz;       // bf16 [T][vc] or f32 hi [T][vc]
+  float* dz_lo;   // [T][vc]
+  float* dzt_hi;  // [vc][ldT]
+  float* dzt_lo;
+  float* acc;     // bf16 path, [T][H] when more than one slab
+  float *x_hi, *x_lo, *xt_hi, *xt_lo;  // [T][H], [H][ldT]
+  float *w_hi, *w_lo, *wt_hi, *wt_lo;  // [V][H], [H][ldV]
+};
+
+size_t carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, BwdWs* w) {
+  BwdWs r{};
+  r.vc = slab_width(T, V, dtype);
+  r.n_slabs = cdiv(V, r.vc);
+  r.ldT = round_up(T, 4);
+  r.ldV = round_up(V, 4);
+  if (dtype == FLCE_DTYPE_BF16) {
+    r.dz = c.take(size_t(2) * T * r.vc);
+    if (r.n_slabs > 1) r.acc = static_cast<float*>(c.take(sizeof(float) * T * H));
+  } else {
+    r.dz = c.take(sizeof(float) * T * r.vc);
+    r.dz_lo = static_cast<float*>(c.take(sizeof(float) * T * r.vc));
+    r.dzt_hi = static_cast<float*>(c.take(sizeof(float) * r.vc * r.ldT));
+    r.dzt_lo = static_cast<float*>(c.take(sizeof(float) * r.vc * r.ldT));
+    r.x_hi = static_cast<float*>(c.take(sizeof(float) * T * H));
+    r.x_lo = static_cast<float*>(c.take(sizeof(float) * T * H));
+    r.xt_hi = static_cast<float*>(c.take(sizeof(float) * H * r.ldT));
+    r.xt_lo = static_cast<float*>(c.take(sizeof(float) * H * r.ldT));
+    r.w_hi = static_cast<float*>(c.take(sizeof(float) * V * H));
+    r.w_lo = static_cast<float*>(c.take(sizeof(float) * V * H));
+    r.wt_hi = static_cast<float*>(c.take(sizeof(float) * H * r.ldV));
+    r.wt_lo = static_cast<float*>(c.take(sizeof(float) * H * r.ldV));
+  }
+  if (w) *w = r;
+  return c.off;
+}
+
+struct Range {
+  uintptr_t lo, hi;
+};
+inline Range rng(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + bytes};
+}
+inline bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_device(flce::Device* dev) {
+  if (!flce::current_device(dev)) return FLCE_ERR_CUDA;
+  if (dev->cc_major != 10 || dev->cc_minor != 3) return FLCE_ERR_UNSUPPORTED;
+  return FLCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int flce_version(void) { return 10000; }
+
+const char* flce_strerror(int code) {
+  switch (code) {
+    case FLCE_OK: return "ok";
+    case FLCE_ERR_ARG: return "invalid argument (null pointer, size out of range or unknown enum)";
+    case FLCE_ERR_UNSUPPORTED:
+      return "unsupported (misaligned pointer or row stride, or device is not sm_103)";
+    case FLCE_ERR_WORKSPACE: return "workspace missing or smaller than the size query requires";
+    case FLCE_ERR_ALIAS: return "an output overlaps an input or another output";
+    case FLCE_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    default: return "unknown error code";
+  }
+}
+
+size_t flce_forward_workspace_size(int64_t T, int64_t H, int64_t V, int dtype) {
+  if (!dims_ok(T, H, V, dtype)) return 0;
+  Carver c;
+  return carve_fwd(c, T, H, V, dtype, nullptr);
+}
+
+size_t flce_backward_workspace_size(int64_t T, int64_t H, int64_t V, int dtype) {
+  if (!dims_ok(T, H, V, dtype)) return 0;
+  Carver c;
+  return carve_bwd(c, T, H, V, dtype, nullptr);
+}
+
+int64_t flce_backward_slab_width(int64_t T, int64_t H, int64_t V, int dtype) {
+  if (!dims_ok(T, H, V, dtype)) return 0;
+  return slab_width(T, V, dtype);
+}
+
+int flce_timing_enable(int on) {
+  std::lock_guard<std::mutex> lock(flce::g_timing_mu);
+  flce::g_timing_on = on != 0;
+  return FLCE_OK;
+}
+
+int flce_timing_read(int64_t counts[4], double ms[4]) {
+  if (!counts || !ms) return FLCE_ERR_ARG;
+  std::vector<flce::TimedLaunch> done;
+  {
+    std::lock_guard<std::mutex> lock(flce::g_timing_mu);
+    done.swap(flce::g_pending);
+  }
+  for (int r = 0; r < 4; ++r) {
+    counts[r] = 0;
+    ms[r] = 0.0;
+  }
+  int rc = FLCE_OK;
+  for (const auto& t : done) {
+    float el = 0.f;
+    if (cudaEventSynchronize(t.end) != cudaSuccess ||
+        cudaEventElapsedTime(&el, t.begin, t.end) != cudaSuccess) {
+      rc = FLCE_ERR_CUDA;
+      continue;
+    }
+    if (t.role >= 0 && t.role < 4) {
+      counts[t.role] += 1;
+      ms[t.role] += el;
+    }
+  }
+  std::lock_guard<std::mutex> lock(flce::g_timing_mu);
+  for (const auto& t : done) {
+    flce::g_event_pool.push_back(t.begin);
+    flce::g_event_pool.push_back(t.end);
+  }
+  return rc;
+}
+
+int flce_set_backward_slab_width(int64_t vc) {
+  if (vc < 0 || vc % kTileN != 0 || vc > kMaxDim) return FLCE_ERR_ARG;
+  g_slab_override.store(vc);
+  return FLCE_OK;
+}
+
+int flce_forward(const void* x, const void* weight, const int64_t* target, int64_t T, int64_t H,
+                 int64_t V, int dtype, int reduction, float* loss, float* lse, void* workspace,
+                 size_t workspace_bytes, int* status, void* stream) {
+  // ---- host-side validation (no CUDA call before this block passes)
+  if (!x || !weight || !target || !loss || !lse || !status) return FLCE_ERR_ARG;
+  if (!dims_ok(T, H, V, dtype)) return FLCE_ERR_ARG;
+  if (reduction != FLCE_REDUCTION_SUM && reduction != FLCE_REDUCTION_MEAN) return FLCE_ERR_ARG;
+  const int eb = elem_bytes(dtype);
+  if ((H * eb) % 16 != 0 || !aligned16(x) || !aligned16(weight)) return FLCE_ERR_UNSUPPORTED;
+  const size_t need = flce_forward_workspace_size(T, H, V, dtype);
+  if (!workspace || workspace_bytes < need) return FLCE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return FLCE_ERR_UNSUPPORTED;
+  const Range in[3] = {rng(x, size_t(T) * H * eb), rng(weight, size_t(V) * H * eb),
+                       rng(target, size_t(T) * 8)};
+  const Range out[4] = {rng(loss, 4), rng(lse, size_t(T) * 4), rng(workspace, need),
+                        rng(status, sizeof(int))};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlap(out[i], in[j])) return FLCE_ERR_ALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(out[i], out[j])) return FLCE_ERR_ALIAS;
+  }
+
+  flce::Device dev;
+  int rc = check_device(&dev);
+  if (rc != FLCE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  Carver c;
+  c.base = static_cast<uint8_t*>(workspace);
+  FwdWs w;
+  carve_fwd(c, T, H, V, dtype, &w);
+
+  flce::FwdLaunch p{};
+  p.target = target;
+  p.part_m = w.part_m;
+  p.part_s = w.part_s;
+  p.zy = w.zy;
+  p.block_sums = w.block_sums;
+  p.lse = lse;
+  p.loss = loss;
+  p.status = status;
+  p.T = int(T);
+  p.H = int(H);
+  p.V = int(V);
+  p.reduction = reduction;
+  p.sms = dev.sms;
+  p.stream = s;
+
+  cudaError_t e;
+  if (dtype == FLCE_DTYPE_BF16) {
+    CUtensorMap tx, tw;
+    if (!flce::make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, H, T, H * 2, 64, kTileM) ||
+        !flce::make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, weight, H, V, H * 2, 64, kTileN))
+      return FLCE_ERR_CUDA;
+    e = flce::timed_launch(0, s, [&] { return flce::launch_forward_bf16(tx, tw, p); });
+  } else {
+    CUtensorMap txh, txl, twh, twl;
+    const auto F = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (!flce::make_tmap_2d(&txh, F, w.x_hi, H, T, H * 4, 32, kTileM) ||
+        !flce::make_tmap_2d(&txl, F, w.x_lo, H, T, H * 4, 32, kTileM) ||
+        !flce::make_tmap_2d(&twh, F, w.w_hi, H, V, H * 4, 32, kTileN) ||
+        !flce::make_tmap_2d(&twl, F, w.w_lo, H, V, H * 4, 32, kTileN))
+      return FLCE_ERR_CUDA;
+    e = flce::launch_split_tf32(static_cast<const float*>(x), T, H, H, w.x_hi, w.x_lo, false, s);
+    if (e == cudaSuccess)
+      e = flce::launch_split_tf32(static_cast<const float*>(weight), V, H, H, w.w_hi, w.w_lo,
+                                  false, s);
+    if (e == cudaSuccess)
+      e = flce::timed_launch(0, s, [&] { return flce::launch_forward_tf32(txh, twh, txl, twl, p); });
+  }
+  return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
+}
+
+int flce_backward(const void* x, const void* weight, const int64_t* target, const float* lse,
+                  int64_t T, int64_t H, int64_t V, int dtype, int reduction,
+                  const float* grad_loss, void* grad_x, void* grad_weight, void* workspace,
+                  size_t workspace_bytes, int* status, void* stream) {
+  if (!x || !weight || !target || !lse || !grad_loss || !grad_x || !grad_weight || !status)
+    return FLCE_ERR_ARG;
+  if (!dims_ok(T, H, V, dtype)) return FLCE_ERR_ARG;
+  if (reduction != FLCE_REDUCTION_SUM && reduction != FLCE_REDUCTION_MEAN) return FLCE_ERR_ARG;
+  const int eb = elem_bytes(dtype);
+  if ((H * eb) % 16 != 0 || !aligned16(x) || !aligned16(weight) || !aligned16(grad_x) ||
+      !aligned16(grad_weight))
+    return FLCE_ERR_UNSUPPORTED;
+  const size_t need = flce_backward_workspace_size(T, H, V, dtype);
+  if (!workspace || workspace_bytes < need) return FLCE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return FLCE_ERR_UNSUPPORTED;
+  const Range in[5] = {rng(x, size_t(T) * H * eb), rng(weight, size_t(V) * H * eb),
+                       rng(target, size_t(T) * 8), rng(lse, size_t(T) * 4), rng(grad_loss, 4)};
+  const Range out[4] = {rng(grad_x, size_t(T) * H * eb), rng(grad_weight, size_t(V) * H * eb),
+                        rng(workspace, need), rng(status, sizeof(int))};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 5; ++j)
+      if (overlap(out[i], in[j])) return FLCE_ERR_ALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(out[i], out[j])) return FLCE_ERR_ALIAS;
+  }
+
+  flce::Device dev;
+  int rc = check_device(&dev);
+  if (rc != FLCE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  Carver c;
+  c.base = static_cast<uint8_t*>(workspace);
+  BwdWs w;
+  carve_bwd(c, T, H, V, dtype, &w);
+  const float scale = reduction == FLCE_REDUCTION_MEAN ? 1.0f / float(T) : 1.0f;
+  const bool bf16 = dtype == FLCE_DTYPE_BF16;
+  const auto DT = bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const uint32_t bk = bf16 ? 64 : 32;  // elements per 128-byte swizzle row
+
+  cudaError_t e = cudaSuccess;
+  // Slab-invariant operand maps.
+  CUtensorMap tx, tx_mn, txh, txl, txth, txtl;
+  if (bf16) {
+    if (!flce::make_tmap_2d(&tx, DT, x, H, T, H * 2, bk, kTileM) ||
+        !flce::make_tmap_2d(&tx_mn, DT, x, H, T, H * 2, 64, 64))
+      return FLCE_ERR_CUDA;
+  } else {
+    if (!flce::make_tmap_2d(&txh, DT, w.x_hi, H, T, H * 4, bk, kTileM) ||
+        !flce::make_tmap_2d(&txl, DT, w.x_lo, H, T, H * 4, bk, kTileM) ||
+        !flce::make_tmap_2d(&txth, DT, w.xt_hi, T, H, w.ldT * 4, bk, kTileN) ||
+        !flce::make_tmap_2d(&txtl, DT, w.xt_lo, T, H, w.ldT * 4, bk, kTileN))
+      return FLCE_ERR_CUDA;
+    const float* xf = static_cast<const float*>(x);
+    const float* wf = static_cast<const float*>(weight);
+    e = flce::launch_split_tf32(xf, T, H, H, w.x_hi, w.x_lo, false, s);
+    if (e == cudaSuccess) e = flce::launch_split_tf32(xf, T, H, w.ldT, w.xt_hi, w.xt_lo, true, s);
+    if (e == cudaSuccess) e = flce::launch_split_tf32(wf, V, H, H, w.w_hi, w.w_lo, false, s);
+    if (e == cudaSuccess) e = flce::launch_split_tf32(wf, V, H, w.ldV, w.wt_hi, w.wt_lo, true, s);
+    if (e != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+
+  for (int64_t si = 0; si < w.n_slabs && e == cudaSuccess; ++si) {
+    const int64_t slab0 = si * w.vc;
+    const int64_t sw = (V - slab0) < w.vc ? (V - slab0) : w.vc;
+    const int mode = w.n_slabs == 1 ? 0 : (si == 0 ? 1 : (si == w.n_slabs - 1 ? 3 : 2));
+
+    flce::DzLaunch dz{};
+    dz.target = target;
+    dz.lse = lse;
+    dz.grad_loss = grad_loss;
+    dz.scale = scale;
+    dz.dz = w.dz;
+    dz.dz_lo = w.dz_lo;
+    dz.dzt_hi = w.dzt_hi;
+    dz.dzt_lo = w.dzt_lo;
+    dz.ldz = int(w.vc);
+    dz.ldt = int(w.ldT);
+    dz.T = int(T);
+    dz.H = int(H);
+    dz.slab0 = int(slab0);
+    dz.slab_w = int(sw);
+    dz.status = status;
+    dz.sms = dev.sms;
+    dz.stream = s;
+
+    flce::GradWLaunch gw{};
+    gw.grad_w = grad_weight;
+    gw.H = int(H);
+    gw.T = int(T);
+    gw.slab0 = int(slab0);
+    gw.slab_w = int(sw);
+    gw.status = status;
+    gw.sms = dev.sms;
+    gw.stream = s;
+
+    flce::GradXLaunch gx{};
+    gx.acc = bf16 ? w.acc : static_cast<float*>(grad_x);
+    gx.grad_x = grad_x;
+    gx.mode = mode;
+    gx.T = int(T);
+    gx.H = int(H);
+    gx.K = int(sw);
+    gx.status = status;
+    gx.sms = dev.sms;
+    gx.stream = s;
+
+    if (bf16) {
+      const uint8_t* wslab = static_cast<const uint8_t*>(weight) + size_t(slab0) * H * 2;
+      CUtensorMap tws, tdz_mn, tdz_k, tw_mn;
+      if (!flce::make_tmap_2d(&tws, DT, wslab, H, sw, H * 2, bk, kTileN) ||
+          !flce::make_tmap_2d(&tdz_mn, DT, w.dz, sw, T, w.vc * 2, 64, 64) ||
+          !flce::make_tmap_2d(&tdz_k, DT, w.dz, sw, T, w.vc * 2, bk, kTileM) ||
+          !flce::make_tmap_2d(&tw_mn, DT, wslab, H, sw, H * 2, 64, 64))
+        return FLCE_ERR_CUDA;
+      e = flce::timed_launch(1, s, [&] { return flce::launch_dz_bf16(tx, tws, dz); });
+      if (e == cudaSuccess)
+        e = flce::timed_launch(2, s, [&] { return flce::launch_gradw_bf16(tdz_mn, tx_mn, gw); });
+      if (e == cudaSuccess)
+        e = flce::timed_launch(3, s, [&] { return flce::launch_gradx_bf16(tdz_k, tw_mn, gx); });
+    } else {
+      CUtensorMap twh, twl, tdzth, tdztl, tdzh, tdzl, twth, twtl;
+      if (!flce::make_tmap_2d(&twh, DT, w.w_hi + size_t(slab0) * H, H, sw, H * 4, bk, kTileN) ||
+          !flce::make_tmap_2d(&twl, DT, w.w_lo + size_t(slab0) * H, H, sw, H * 4, bk, kTileN) ||
+          !flce::make_tmap_2d(&tdzth, DT, w.dzt_hi, T, sw, w.ldT * 4, bk, kTileM) ||
+          !flce::make_tmap_2d(&tdztl, DT, w.dzt_lo, T, sw, w.ldT * 4, bk, kTileM) ||
+          !flce::make_tmap_2d(&tdzh, DT, w.dz, sw, T, w.vc * 4, bk, kTileM) ||
+          !flce::make_tmap_2d(&tdzl, DT, w.dz_lo, sw, T, w.vc * 4, bk, kTileM) ||
+          !flce::make_tmap_2d(&twth, DT, w.wt_hi + slab0, sw, H, w.ldV * 4, bk, kTileN) ||
+          !flce::make_tmap_2d(&twtl, DT, w.wt_lo + slab0, sw, H, w.ldV * 4, bk, kTileN))
+        return FLCE_ERR_CUDA;
+      e = flce::timed_launch(1, s, [&] { return flce::launch_dz_tf32(txh, twh, txl, twl, dz); });
+      if (e == cudaSuccess)
+        e = flce::timed_launch(2, s, [&] { return flce::launch_gradw_tf32(tdzth, txth, tdztl, txtl, gw); });
+      if (e == cudaSuccess)
+        e = flce::timed_launch(3, s, [&] { return flce::launch_gradx_tf32(tdzh, twth, tdzl, twtl, gx); });
+    }
+  }
+  return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,117 @@
+// flce_fwd.cu - forward kernels: the fused projection + online log-sum-exp contraction, the
+// fixed-order merge of its per-vocab-tile partials into lse[T], and the deterministic loss
+// reduction.
+#include "epilogues.cuh"
+#include "flce_internal.h"
+
+namespace flce {
+
+constexpr int kCombineThreads = 256;
+
+// Merge the per-(vocab tile) partials of each token in increasing tile order:
+//   M = max_i m_i,  S = sum_i s_i exp(m_i - M),  lse = M + ln S,  l = lse - z[t, target[t]].
+// Writes lse[t] and one partial loss sum per block (fixed-order tree).
+__global__ void __launch_bounds__(kCombineThreads)
+    k_fwd_combine(const float* __restrict__ part_m, const float* __restrict__ part_s,
+                  const float* __restrict__ zy, const int64_t* __restrict__ target, int T, int V,
+                  int n_tiles, float* __restrict__ lse, float* __restrict__ block_sums,
+                  int* status) {
+  const int t = blockIdx.x * kCombineThreads + threadIdx.x;
+  float l = 0.f;
+  if (t < T) {
+    float M = -INFINITY, S = 0.f;
+    for (int i = 0; i < n_tiles; ++i) {
+      const float m = part_m[static_cast<size_t>(i) * T + t];
+      const float s = part_s[static_cast<size_t>(i) * T + t];
+      const float mn = fmaxf(M, m);
+      S = S * ex2((M - mn) * kLog2e) + s * ex2((m - mn) * kLog2e);
+      M = mn;
+    }
+    const float lse_t = M + logf(S);
+    lse[t] = lse_t;
+    const int64_t y = target[t];
+    if (y < 0 || y >= V) {
+      atomicOr(status, FLCE_STATUS_TARGET_RANGE);
+      l = __int_as_float(0x7fc00000);  // NaN
+    } else {
+      l = lse_t - zy[t];
+    }
+  }
+  // Fixed-order block reduction: shuffle tree within each warp, then over the warp sums.
+  __shared__ float warp_sums[kCombineThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_down_sync(0xffffffffu, l, o);
+  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = l;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float w = threadIdx.x < kCombineThreads / 32 ? warp_sums[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w += __shfl_down_sync(0xffffffffu, w, o);
+    if (threadIdx.x == 0) block_sums[blockIdx.x] = w;
+  }
+}
+
+// loss = sum of the block sums (fp64, fixed order), divided by T for the mean reduction.
+__global__ void __launch_bounds__(256)
+    k_fwd_finalize(const float* __restrict__ block_sums, int n, int T, int reduction,
+                   float* __restrict__ loss) {
+  __shared__ double part[256];
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < n; i += 256) acc += static_cast<double>(block_sums[i]);
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    double total = part[0];
+    if (reduction == FLCE_REDUCTION_MEAN) total /= static_cast<double>(T);
+    loss[0] = static_cast<float>(total);
+  }
+}
+
+template <bool kTF32>
+static cudaError_t launch_forward(const CUtensorMap& tx, const CUtensorMap& tw,
+                                  const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
+                                  const FwdLaunch& p) {
+  using G = StageGeom<kTF32>;
+  auto kern = k_umma_gemm<false, false, kTF32, FwdEpi>;
+  // Per-device attribute; cheap enough to set on every call.
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  GemmGrid g;
+  g.m_tiles = (p.T + kBM - 1) / kBM;
+  g.n_tiles = (p.V + kBN - 1) / kBN;
+  g.k_blocks = (p.H + G::kBK - 1) / G::kBK;
+  g.group_m = kGroupM;
+  g.status = p.status;
+  FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V};
+  const int tiles = g.m_tiles * g.n_tiles;
+  const int grid = tiles < p.sms ? tiles : p.sms;
+  kern<<<grid, kThreads, G::kSmemBytes, p.stream>>>(tx, tw, tx_lo, tw_lo, g, ea);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const int nblk = (p.T + kCombineThreads - 1) / kCombineThreads;
+  k_fwd_combine<<<nblk, kCombineThreads, 0, p.stream>>>(p.part_m, p.part_s, p.zy, p.target, p.T,
+                                                        p.V, g.n_tiles, p.lse, p.block_sums,
+                                                        p.status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_fwd_finalize<<<1, 256, 0, p.stream>>>(p.block_sums, nblk, p.T, p.reduction, p.loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_forward_bf16(const CUtensorMap& tx, const CUtensorMap& tw, const FwdLaunch& p) {
+  return launch_forward<false>(tx, tw, tx, tw, p);
+}
+
+cudaError_t launch_forward_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
+                                const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
+                                const FwdLaunch& p) {
+  return launch_forward<true>(tx_hi, tw_hi, tx_lo, tw_lo, p);
+}
+
+}  // namespace flce

@@ -1,0 +1,112 @@
+// flce_internal.h - host-side declarations shared by the libflce translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/flce.h"
+
+namespace flce {
+
+// Tile sizes of the contraction core (see gemm.cuh).
+constexpr int kTileM = 128;
+constexpr int kTileN = 256;
+
+// Raster group (consecutive M tiles that walk N together) for L2 reuse of the B operand.
+constexpr int kGroupM = 16;
+
+struct Device {
+  int id = -1;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+
+// Device properties of the current device (cached per device id). Returns false on CUDA error.
+bool current_device(Device* d);
+
+// 2-D tensor map with 128-byte swizzle, zero fill outside [0,inner) x [0,outer).
+//   base: global address (16-byte aligned), inner/outer: extents in elements / rows,
+//   row_bytes: stride between rows (multiple of 16), box_inner x box_outer: box in elements.
+bool make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// ---------------------------------------------------------------- forward launchers (flce_fwd.cu)
+struct FwdLaunch {
+  const int64_t* target;
+  float* part_m;      // [n_tiles][T]
+  float* part_s;      // [n_tiles][T]
+  float* zy;          // [T]
+  float* block_sums;  // [ceil(T / 256)]
+  float* lse;         // [T]
+  float* loss;        // [1]
+  int* status;
+  int T, H, V, reduction;
+  int sms;
+  cudaStream_t stream;
+};
+// x/W maps: K-major boxes {64 x 128} (x) and {64 x 256} (W); tf32 adds lo copies.
+cudaError_t launch_forward_bf16(const CUtensorMap& tx, const CUtensorMap& tw, const FwdLaunch& p);
+cudaError_t launch_forward_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
+                                const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
+                                const FwdLaunch& p);
+
+// ---------------------------------------------------------------- backward launchers (flce_bwd.cu)
+struct DzLaunch {
+  const int64_t* target;
+  const float* lse;
+  const float* grad_loss;
+  float scale;        // 1 (sum) or 1/T (mean)
+  void* dz;           // bf16 [T][ldz]   or fp32 hi [T][ldz]
+  void* dz_lo;        // fp32 lo [T][ldz] (tf32 path)
+  void* dzt_hi;       // fp32 [Vc][ldt] transposed hi (tf32 path)
+  void* dzt_lo;       // fp32 [Vc][ldt] transposed lo (tf32 path)
+  int ldz, ldt;
+  int T, H, slab0, slab_w;
+  int* status;
+  int sms;
+  cudaStream_t stream;
+};
+cudaError_t launch_dz_bf16(const CUtensorMap& tx, const CUtensorMap& tw_slab, const DzLaunch& p);
+cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
+                           const CUtensorMap& tx_lo, const CUtensorMap& tw_lo, const DzLaunch& p);
+
+struct GradWLaunch {
+  void* grad_w;  // [V][H] (dtype); rows slab0 .. slab0 + slab_w are written
+  int H, T, slab0, slab_w;
+  int* status;
+  int sms;
+  cudaStream_t stream;
+};
+// bf16: A = dz slab (MN-major boxes {64 x 64}), B = x (MN-major boxes {64 x 64}).
+cudaError_t launch_gradw_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
+                              const GradWLaunch& p);
+// tf32: A = dz^T slab (K-major, hi/lo), B = x^T (K-major, hi/lo).
+cudaError_t launch_gradw_tf32(const CUtensorMap& tdzt_hi, const CUtensorMap& txt_hi,
+                              const CUtensorMap& tdzt_lo, const CUtensorMap& txt_lo,
+                              const GradWLaunch& p);
+
+struct GradXLaunch {
+  float* acc;    // fp32 [T][H] accumulator (bf16 path) or the fp32 output itself
+  void* grad_x;  // [T][H] (dtype)
+  int mode;      // 0 only slab, 1 first, 2 middle, 3 last
+  int T, H, K;
+  int* status;
+  int sms;
+  cudaStream_t stream;
+};
+// bf16: A = dz slab (K-major {64 x 128}), B = W slab (MN-major {64 x 64}).
+cudaError_t launch_gradx_bf16(const CUtensorMap& tdz_k, const CUtensorMap& tw_mn,
+                              const GradXLaunch& p);
+// tf32: A = dz slab (K-major hi/lo), B = W^T slab (K-major hi/lo).
+cudaError_t launch_gradx_tf32(const CUtensorMap& tdz_hi, const CUtensorMap& twt_hi,
+                              const CUtensorMap& tdz_lo, const CUtensorMap& twt_lo,
+                              const GradXLaunch& p);
+
+// fp32 -> (hi, lo) TF32 split, optionally transposed: src [rows][cols] -> hi/lo [rows][ld_out]
+// or, with transpose, hi/lo [cols][ld_out] (ld_out >= rows).
+cudaError_t launch_split_tf32(const float* src, int64_t rows, int64_t cols, int64_t ld_out,
+                              float* hi, float* lo, bool transpose, cudaStream_t stream);
+
+}  // namespace flce

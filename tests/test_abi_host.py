@@ -1,0 +1,157 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every declared symbol, and
+rejects bad arguments with the documented codes before touching the GPU.
+
+Pointers passed here are fake addresses; every call below must fail validation before any
+CUDA call, so nothing is dereferenced.
+"""
+import os
+import re
+import subprocess
+
+import pytest
+
+from lm_head_linear_02_gb300 import binding as B
+from lm_head_linear_02_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flce_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "flce_forward" in names and "flce_backward" in names
+    out = subprocess.run(["nm", "-D", "--defined-only", B.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (flce_[a-z_0-9]+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(lib, n)
+
+
+def test_version_and_strerror(lib):
+    assert B.flce_version() == 10000
+    for code in (0, -1, -2, -3, -4, -5):
+        assert B.flce_strerror(code)
+    assert "unknown" in B.flce_strerror(-99)
+
+
+def test_workspace_sizes():
+    T, H, V = 16384, 4096, 128256
+    fwd = B.flce_forward_workspace_size(T, H, V, B.FLCE_DTYPE_BF16)
+    n_tiles = (V + 255) // 256
+    assert fwd >= 2 * 4 * n_tiles * T + 4 * T
+    bwd = B.flce_backward_workspace_size(T, H, V, B.FLCE_DTYPE_BF16)
+    vc = B.flce_backward_slab_width(T, H, V, B.FLCE_DTYPE_BF16)
+    assert vc % 256 == 0 and 256 <= vc <= V + 255
+    assert bwd >= 2 * T * vc
+    # never anything close to the tokens x vocab logits
+    assert fwd + bwd < 2 * T * V
+    for bad in [(0, H, V, 0), (T, 0, V, 0), (T, H, -1, 0), (T, H, V, 7)]:
+        assert B.flce_forward_workspace_size(*bad) == 0
+        assert B.flce_backward_workspace_size(*bad) == 0
+
+
+def test_workspace_stays_below_logits_size_at_32k_tokens():
+    T, H, V = 32768, 4096, 128256
+    logits_bf16 = 2 * T * V
+    fwd = B.flce_forward_workspace_size(T, H, V, B.FLCE_DTYPE_BF16)
+    bwd = B.flce_backward_workspace_size(T, H, V, B.FLCE_DTYPE_BF16)
+    inputs_outputs = 2 * (2 * T * H + 2 * V * H) + 8 * T + 4 * T
+    assert inputs_outputs + max(fwd, bwd) < logits_bf16
+
+
+def test_slab_override(lib):
+    try:
+        B.flce_set_backward_slab_width(512)
+        assert B.flce_backward_slab_width(1000, 64, 10000, 0) == 512
+        assert B.flce_backward_slab_width(1000, 64, 300, 0) == 512  # clamped to round_up(V)
+        with pytest.raises(B.FlceError):
+            B.flce_set_backward_slab_width(100)
+    finally:
+        B.flce_set_backward_slab_width(0)
+    assert B.flce_backward_slab_width(1000, 64, 300, 0) == 512
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+def _fwd(**kw):
+    a = dict(x=FAKE, weight=FAKE + 0x10000000, target=FAKE + 0x20000000, T=64, H=64, V=512,
+             dtype=0, reduction=1, loss=FAKE + 0x30000000, lse=FAKE + 0x30001000,
+             workspace=FAKE + 0x40000000, workspace_bytes=1 << 30, status=FAKE + 0x30000100,
+             stream=0)
+    a.update(kw)
+    return B.flce_forward(a["x"], a["weight"], a["target"], a["T"], a["H"], a["V"], a["dtype"],
+                          a["reduction"], a["loss"], a["lse"], a["workspace"],
+                          a["workspace_bytes"], a["status"], a["stream"], check=False)
+
+
+def _bwd(**kw):
+    a = dict(x=FAKE, weight=FAKE + 0x10000000, target=FAKE + 0x20000000,
+             lse=FAKE + 0x21000000, T=64, H=64, V=512, dtype=0, reduction=1,
+             grad_loss=FAKE + 0x22000000, grad_x=FAKE + 0x30000000,
+             grad_weight=FAKE + 0x31000000, workspace=FAKE + 0x40000000,
+             workspace_bytes=1 << 30, status=FAKE + 0x32000000, stream=0)
+    a.update(kw)
+    return B.flce_backward(a["x"], a["weight"], a["target"], a["lse"], a["T"], a["H"], a["V"],
+                           a["dtype"], a["reduction"], a["grad_loss"], a["grad_x"],
+                           a["grad_weight"], a["workspace"], a["workspace_bytes"], a["status"],
+                           a["stream"], check=False)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=0), B.FLCE_ERR_ARG),
+    (dict(target=0), B.FLCE_ERR_ARG),
+    (dict(loss=0), B.FLCE_ERR_ARG),
+    (dict(status=0), B.FLCE_ERR_ARG),
+    (dict(T=0), B.FLCE_ERR_ARG),
+    (dict(V=-3), B.FLCE_ERR_ARG),
+    (dict(T=1 << 30), B.FLCE_ERR_ARG),
+    (dict(dtype=2), B.FLCE_ERR_ARG),
+    (dict(reduction=2), B.FLCE_ERR_ARG),
+    (dict(H=60), B.FLCE_ERR_UNSUPPORTED),          # 120-byte rows for bf16
+    (dict(H=6, dtype=1), B.FLCE_ERR_UNSUPPORTED),  # 24-byte rows for f32
+    (dict(x=FAKE + 8), B.FLCE_ERR_UNSUPPORTED),
+    (dict(workspace=0), B.FLCE_ERR_WORKSPACE),
+    (dict(workspace_bytes=16), B.FLCE_ERR_WORKSPACE),
+    (dict(workspace=FAKE + 0x40000010), B.FLCE_ERR_UNSUPPORTED),
+    (dict(lse=FAKE + 0x100), B.FLCE_ERR_ALIAS),     # lse overlaps x
+    (dict(loss=FAKE + 0x30001004), B.FLCE_ERR_ALIAS),  # loss inside lse
+    (dict(workspace=FAKE + 0x10000000), B.FLCE_ERR_ALIAS),  # workspace over weight
+])
+def test_forward_validation(lib, kw, code):
+    assert _fwd(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(lse=0), B.FLCE_ERR_ARG),
+    (dict(grad_loss=0), B.FLCE_ERR_ARG),
+    (dict(grad_weight=0), B.FLCE_ERR_ARG),
+    (dict(H=4), B.FLCE_ERR_UNSUPPORTED),
+    (dict(grad_x=FAKE + 0x30000004), B.FLCE_ERR_UNSUPPORTED),
+    (dict(workspace_bytes=0), B.FLCE_ERR_WORKSPACE),
+    (dict(grad_x=FAKE + 0x10), B.FLCE_ERR_ALIAS),           # grad_x over x
+    (dict(grad_weight=FAKE + 0x30000000), B.FLCE_ERR_ALIAS),  # the two outputs overlap
+    (dict(status=FAKE + 0x21000000), B.FLCE_ERR_ALIAS),      # status inside lse
+])
+def test_backward_validation(lib, kw, code):
+    assert _bwd(**kw) == code
+
+
+def test_binding_raises_on_error(lib):
+    with pytest.raises(B.FlceError) as e:
+        B.flce_forward(0, 0, 0, 1, 8, 8, 0, 0, 0, 0, 0, 0, 0, 0)
+    assert e.value.code == B.FLCE_ERR_ARG
