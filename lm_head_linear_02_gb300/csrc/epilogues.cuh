@@ -129,16 +129,16 @@ struct FwdEpi {
 
 // ------------------------------------------------------------------------------- backward dz
 // "[example] fused_linear_cross_entropy kernel" (Helion PR #1268), backward: the logits are
-// recomputed and turned into dz = (softmax - onehot(target)) * g in registers; here they are
-// written to a bounded vocab slab (T x Vc) that feeds the two gradient contractions.
-// Columns outside the slab are stored as 0; rows >= T are not stored.
+// recomputed and turned into dz = (softmax - onehot(target)) * g in registers; here the
+// unscaled factor (softmax - onehot), whose entries lie in [-1, 1], is written to a bounded
+// vocab slab (T x Vc) that feeds the two gradient contractions, and g is applied in fp32 in
+// their epilogues. Keeping g out of the bf16 slab keeps the dominant -1 entries exact for any
+// reduction. Columns outside the slab are stored as 0; rows >= T are not stored.
 template <bool kTF32>
 struct DzEpi {
   struct Args {
     const int64_t* target;
     const float* lse;
-    const float* grad_loss;
-    float scale;
     void* dz;      // bf16 [T][ldz] or fp32 hi [T][ldz]
     float* dz_lo;  // fp32 lo [T][ldz]          (tf32)
     float* dzt_hi; // fp32 [slab_w][ldt]        (tf32)
@@ -146,14 +146,10 @@ struct DzEpi {
     int ldz, ldt;
     int T, slab0, slab_w;
   };
-  struct State {
-    float g;
-  };
-  static __device__ __forceinline__ void init(const Args& a, State& st) {
-    st.g = __ldg(a.grad_loss) * a.scale;
-  }
+  struct State {};
+  static __device__ __forceinline__ void init(const Args&, State&) {}
 
-  static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
+  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
                                               uint32_t taddr) {
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
@@ -161,7 +157,6 @@ struct DzEpi {
     const long long y = valid ? static_cast<long long>(__ldg(a.target + t)) : -1ll;
     const int n0 = nb * kBN;  // slab-relative column of the tile
     const long long rel = y - a.slab0 - n0;
-    const float g = st.g;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
       const int c0 = n0 + c * 32;
@@ -170,8 +165,8 @@ struct DzEpi {
       load_chunk(taddr, c, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float d = ex2(fmaf(v[j], kLog2e, -lsel)) * g;
-        if (rel == c * 32 + j) d -= g;
+        float d = ex2(fmaf(v[j], kLog2e, -lsel));
+        if (rel == c * 32 + j) d -= 1.0f;
         if (c0 + j >= a.slab_w) d = 0.f;
         v[j] = d;
       }
@@ -202,16 +197,24 @@ struct DzEpi {
 // ------------------------------------------------------------------------------- grad_weight
 // grad_weight[slab rows, :] = dz_slab^T . x : the contraction runs over all T tokens, so each
 // output tile is complete when it leaves TMEM and is written exactly once.
+// The accumulator holds (softmax - onehot)^T . x; the gradient scale g = grad_loss (sum) or
+// grad_loss / T (mean) is applied here in fp32.
 template <bool kF32Out>
 struct GradWEpi {
   struct Args {
     void* grad_w;  // [V][H]
+    const float* grad_loss;
+    float scale;
     int H, slab0, slab_w;
   };
-  struct State {};
-  static __device__ __forceinline__ void init(const Args&, State&) {}
+  struct State {
+    float g;
+  };
+  static __device__ __forceinline__ void init(const Args& a, State& st) {
+    st.g = __ldg(a.grad_loss) * a.scale;
+  }
 
-  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
+  static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
                                               uint32_t taddr) {
     const int r = mb * kBM + row;  // slab-relative vocab row
     const bool valid = r < a.slab_w;
@@ -223,6 +226,8 @@ struct GradWEpi {
       float v[32];
       load_chunk(taddr, c, v);
       if (!valid) continue;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= st.g;
       const int n = min(32, a.H - h0);
       if constexpr (kF32Out)
         store_f32x32(reinterpret_cast<float*>(a.grad_w) + vrow * a.H + h0, v, n);
@@ -240,17 +245,24 @@ struct GradWEpi {
 //   mode 2: middle slab -> acc += D
 //   mode 3: last slab   -> out = acc + D
 // For fp32 outputs `acc` and `out` are the same buffer.
+// As for grad_W, the slab product is scaled by g in fp32 before it is accumulated.
 template <bool kF32Out>
 struct GradXEpi {
   struct Args {
     float* acc;   // [T][H] fp32
     void* out;    // [T][H] dtype
+    const float* grad_loss;
+    float scale;
     int T, H, mode;
   };
-  struct State {};
-  static __device__ __forceinline__ void init(const Args&, State&) {}
+  struct State {
+    float g;
+  };
+  static __device__ __forceinline__ void init(const Args& a, State& st) {
+    st.g = __ldg(a.grad_loss) * a.scale;
+  }
 
-  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
+  static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
                                               uint32_t taddr) {
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
@@ -263,6 +275,8 @@ struct GradXEpi {
       if (!valid) continue;
       const int n = min(32, a.H - h0);
       const size_t o = static_cast<size_t>(t) * a.H + h0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= st.g;
       if (a.mode >= 2) {
         const float4* s = reinterpret_cast<const float4*>(a.acc + o);
 #pragma unroll

@@ -477,8 +477,6 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
     flce::DzLaunch dz{};
     dz.target = target;
     dz.lse = lse;
-    dz.grad_loss = grad_loss;
-    dz.scale = scale;
     dz.dz = w.dz;
     dz.dz_lo = w.dz_lo;
     dz.dzt_hi = w.dzt_hi;
@@ -495,6 +493,8 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
 
     flce::GradWLaunch gw{};
     gw.grad_w = grad_weight;
+    gw.grad_loss = grad_loss;
+    gw.scale = scale;
     gw.H = int(H);
     gw.T = int(T);
     gw.slab0 = int(slab0);
@@ -506,6 +506,8 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
     flce::GradXLaunch gx{};
     gx.acc = bf16 ? w.acc : static_cast<float*>(grad_x);
     gx.grad_x = grad_x;
+    gx.grad_loss = grad_loss;
+    gx.scale = scale;
     gx.mode = mode;
     gx.T = int(T);
     gx.H = int(H);

@@ -30,8 +30,8 @@ static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const 
 }
 
 cudaError_t launch_dz_bf16(const CUtensorMap& tx, const CUtensorMap& tw_slab, const DzLaunch& p) {
-  typename DzEpi<false>::Args ea{p.target, p.lse, p.grad_loss, p.scale, p.dz,  nullptr,
-                                 nullptr,  nullptr, p.ldz,     p.ldt,  p.T, p.slab0, p.slab_w};
+  typename DzEpi<false>::Args ea{p.target, p.lse, p.dz, nullptr, nullptr, nullptr,
+                                 p.ldz,    p.ldt, p.T,  p.slab0, p.slab_w};
   return run_gemm<false, false, false, DzEpi<false>>(tx, tw_slab, tx, tw_slab, p.T, p.slab_w, p.H,
                                                      p.status, p.sms, p.stream, ea);
 }
@@ -40,8 +40,6 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
                            const CUtensorMap& tx_lo, const CUtensorMap& tw_lo, const DzLaunch& p) {
   typename DzEpi<true>::Args ea{p.target,
                                 p.lse,
-                                p.grad_loss,
-                                p.scale,
                                 p.dz,
                                 static_cast<float*>(p.dz_lo),
                                 static_cast<float*>(p.dzt_hi),
@@ -57,7 +55,7 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
 
 cudaError_t launch_gradw_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
                               const GradWLaunch& p) {
-  typename GradWEpi<false>::Args ea{p.grad_w, p.H, p.slab0, p.slab_w};
+  typename GradWEpi<false>::Args ea{p.grad_w, p.grad_loss, p.scale, p.H, p.slab0, p.slab_w};
   return run_gemm<true, true, false, GradWEpi<false>>(tdz_mn, tx_mn, tdz_mn, tx_mn, p.slab_w, p.H,
                                                       p.T, p.status, p.sms, p.stream, ea);
 }
@@ -65,14 +63,14 @@ cudaError_t launch_gradw_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
 cudaError_t launch_gradw_tf32(const CUtensorMap& tdzt_hi, const CUtensorMap& txt_hi,
                               const CUtensorMap& tdzt_lo, const CUtensorMap& txt_lo,
                               const GradWLaunch& p) {
-  typename GradWEpi<true>::Args ea{p.grad_w, p.H, p.slab0, p.slab_w};
+  typename GradWEpi<true>::Args ea{p.grad_w, p.grad_loss, p.scale, p.H, p.slab0, p.slab_w};
   return run_gemm<false, false, true, GradWEpi<true>>(tdzt_hi, txt_hi, tdzt_lo, txt_lo, p.slab_w,
                                                       p.H, p.T, p.status, p.sms, p.stream, ea);
 }
 
 cudaError_t launch_gradx_bf16(const CUtensorMap& tdz_k, const CUtensorMap& tw_mn,
                               const GradXLaunch& p) {
-  typename GradXEpi<false>::Args ea{p.acc, p.grad_x, p.T, p.H, p.mode};
+  typename GradXEpi<false>::Args ea{p.acc, p.grad_x, p.grad_loss, p.scale, p.T, p.H, p.mode};
   return run_gemm<false, true, false, GradXEpi<false>>(tdz_k, tw_mn, tdz_k, tw_mn, p.T, p.H, p.K,
                                                        p.status, p.sms, p.stream, ea);
 }
@@ -80,7 +78,7 @@ cudaError_t launch_gradx_bf16(const CUtensorMap& tdz_k, const CUtensorMap& tw_mn
 cudaError_t launch_gradx_tf32(const CUtensorMap& tdz_hi, const CUtensorMap& twt_hi,
                               const CUtensorMap& tdz_lo, const CUtensorMap& twt_lo,
                               const GradXLaunch& p) {
-  typename GradXEpi<true>::Args ea{p.acc, p.grad_x, p.T, p.H, p.mode};
+  typename GradXEpi<true>::Args ea{p.acc, p.grad_x, p.grad_loss, p.scale, p.T, p.H, p.mode};
   return run_gemm<false, false, true, GradXEpi<true>>(tdz_hi, twt_hi, tdz_lo, twt_lo, p.T, p.H,
                                                       p.K, p.status, p.sms, p.stream, ea);
 }

@@ -56,9 +56,7 @@ cudaError_t launch_forward_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_
 struct DzLaunch {
   const int64_t* target;
   const float* lse;
-  const float* grad_loss;
-  float scale;        // 1 (sum) or 1/T (mean)
-  void* dz;           // bf16 [T][ldz]   or fp32 hi [T][ldz]
+  void* dz;           // (softmax - onehot): bf16 [T][ldz] or fp32 hi [T][ldz]
   void* dz_lo;        // fp32 lo [T][ldz] (tf32 path)
   void* dzt_hi;       // fp32 [Vc][ldt] transposed hi (tf32 path)
   void* dzt_lo;       // fp32 [Vc][ldt] transposed lo (tf32 path)
@@ -74,6 +72,8 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
 
 struct GradWLaunch {
   void* grad_w;  // [V][H] (dtype); rows slab0 .. slab0 + slab_w are written
+  const float* grad_loss;
+  float scale;   // 1 (sum) or 1/T (mean); g = grad_loss[0] * scale
   int H, T, slab0, slab_w;
   int* status;
   int sms;
@@ -90,6 +90,8 @@ cudaError_t launch_gradw_tf32(const CUtensorMap& tdzt_hi, const CUtensorMap& txt
 struct GradXLaunch {
   float* acc;    // fp32 [T][H] accumulator (bf16 path) or the fp32 output itself
   void* grad_x;  // [T][H] (dtype)
+  const float* grad_loss;
+  float scale;
   int mode;      // 0 only slab, 1 first, 2 middle, 3 last
   int T, H, K;
   int* status;
