@@ -197,7 +197,8 @@ def _sampled_checks(inp, rows, label):
     gx_t, gw_t, status = A.flce_backward(x, w, y, lse_t, g, "mean", status=status)
     torch.cuda.synchronize()
     A.check_status(status)
-    peak_extra = torch.cuda.max_memory_allocated() - base
+    peak_total = torch.cuda.max_memory_allocated()
+    peak_extra = peak_total - base
     loss = loss_t.item()
     lse = lse_t.cpu().numpy().astype(np.float64)
     gx_rows = gx_t[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
@@ -214,27 +215,49 @@ def _sampled_checks(inp, rows, label):
     # expected loss band: logits ~ N(0, 0.0004 H) give E[loss] ~= ln V + 0.0002 H
     band = abs(loss - (math.log(V) + 0.0002 * H)) / loss
     print(f"{label}: lse {e_lse:.3e} gx {e_gx:.3e} loss-vs-lse {rel_loss:.3e} band {band:.3e} "
-          f"peak_extra {peak_extra / 1e9:.3f} GB")
+          f"peak {peak_total / 1e9:.3f} GB (library workspace and outputs {peak_extra / 1e9:.3f} GB)")
     assert e_lse <= tol["lse"] and e_gx <= tol["grad"] and rel_loss <= tol["loss"]
     assert band < 0.02
 
-    # grad_weight properties. (1) every dz row sums to 0, so the vocab-sum of grad_W vanishes;
-    # (2) (W c)^T grad_W a = (grad_x c)^T (x a) for any c, a, because grad_W = dz^T x and
-    # grad_x = dz W; grad_x itself is pinned on the sampled rows above.
+    # grad_weight. (1) Property: every dz row sums to 0, so sum_v grad_W[v, h] = 0 exactly; the
+    # bf16 output rounding (unit roundoff 2^-8) bounds what survives by 2^-8 sum_v |grad_W[v,h]|.
+    # x is bf16-exact and T a power of two, so the rounding errors of the target rows are
+    # correlated (each rounds back to -x/T): only this worst-case bound is valid.
     gw = gw_t.float()
-    gx = gx_t.float()
-    wf = w.float()
+    col = gw.double().sum(0).abs()
+    bound = 2.0 ** -8 * gw.double().abs().sum(0) + 1e-9
+    assert bool((col <= bound).all()), float((col / bound).max())
+    # (2) Element-wise cross-check of both gradients at full size against a plain PyTorch fp32
+    # reference of the same operation (materialised fp32 logits, chunk by chunk on the GPU;
+    # independent of libflce). The sampled-row oracle comparison above is the parity claim;
+    # this covers every grad_weight entry in the benchmark's launch configuration.
     xf = x.float()
-    col = gw.double().sum(0).abs().max().item()
-    assert col <= 1e-2 * gw.abs().max().item(), col
-    gen = torch.Generator(device="cuda").manual_seed(1)
-    for _ in range(4):
-        a = torch.randn(H, 1, device="cuda", generator=gen, dtype=torch.float64)
-        c = torch.randn(H, 1, device="cuda", generator=gen, dtype=torch.float64)
-        lhs = ((wf.double() @ c).T @ (gw.double() @ a)).item()
-        rhs = ((gx.double() @ c).T @ (xf.double() @ a)).item()
-        assert abs(lhs - rhs) <= 2e-2 * max(abs(lhs), abs(rhs)), (lhs, rhs)
-    return peak_extra
+    wf = w.float()
+    yd = y
+    gw_ref = torch.zeros_like(wf)
+    gx_err = 0.0
+    gx_ref_max = 0.0
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        for t0 in range(0, T, 2048):
+            t1 = min(T, t0 + 2048)
+            z = xf[t0:t1] @ wf.T
+            p = torch.softmax(z, dim=1)
+            p[torch.arange(t1 - t0, device="cuda"), yd[t0:t1]] -= 1.0
+            p *= 1.0 / T
+            gw_ref += p.T @ xf[t0:t1]
+            gxr = p @ wf
+            gx_err = max(gx_err, (gx_t[t0:t1].float() - gxr).abs().max().item())
+            gx_ref_max = max(gx_ref_max, gxr.abs().max().item())
+            del z, p, gxr
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    e_gw_full = ((gw - gw_ref).abs().max() / gw_ref.abs().max()).item()
+    e_gx_full = gx_err / gx_ref_max
+    print(f"{label}: full-size fp32 torch cross-check: grad_W {e_gw_full:.3e} grad_x {e_gx_full:.3e}")
+    assert e_gw_full <= tol["grad"] and e_gx_full <= tol["grad"]
+    return peak_total
 
 
 @pytest.mark.parametrize("name", ["llama3_head_t4096", "llama3_head_t8192", "llama3_head_t16384"])
@@ -249,6 +272,7 @@ def test_large_batch_memory_and_sampled():
     inp = make_inputs("llama3_head_t32768")
     T, V = inp.workload.T, inp.workload.V
     rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(5).integers(0, T, 14)]))
-    peak_extra = _sampled_checks(inp, rows, "llama3_head_t32768")
+    peak_total = _sampled_checks(inp, rows, "llama3_head_t32768")
     logits_bytes = 2 * T * V  # the bf16 logits an unfused head would hold: 8.405 GB
-    assert peak_extra < logits_bytes
+    # peak device memory of the whole fwd+bwd, inputs and gradients included
+    assert peak_total < logits_bytes
