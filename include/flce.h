@@ -126,6 +126,30 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
                   const float* grad_loss, void* grad_x, void* grad_weight,
                   void* workspace, size_t workspace_bytes, int* status, void* stream);
 
+/* Size of the device array behind flce_forward_static_scratch (64 MiB). */
+#define FLCE_STATIC_SCRATCH_BYTES (64ull << 20)
+
+/*
+ * Forward without a workspace, for callers that cannot allocate device memory. (The pages
+ * have no counterpart: this is an interface addition of this library.) Some callers have no
+ * device allocator to hand the library a workspace from, e.g. a plain C or foreign-language
+ * host program without a CUDA memory pool, or a service whose device-memory budget is fixed at
+ * start-up and which may not call cudaMalloc while it runs (cudaMalloc can also synchronise the
+ * device). This call computes exactly what flce_forward computes, with the same arguments minus
+ * the workspace, and allocates nothing: its scratch is one file-scope device array of
+ * FLCE_STATIC_SCRATCH_BYTES that every GPU loading the library holds until the process exits.
+ *   - Returns FLCE_ERR_WORKSPACE, enqueuing nothing, when the problem's forward scratch
+ *     (flce_forward_workspace_size) exceeds FLCE_STATIC_SCRATCH_BYTES; bf16 problems up to
+ *     about T = 16700 tokens at V = 128256 fit.
+ *   - All calls on a device share the array and it keeps the last call's contents; nothing in
+ *     it has to start at zero. Calls whose GPU work overlaps (e.g. on unordered streams) race.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ */
+int flce_forward_static_scratch(const void* x, const void* weight, const int64_t* target,
+                                int64_t T, int64_t H, int64_t V, int dtype, int reduction,
+                                float* loss, float* lse, int* status, void* stream);
+
 /* Per-launch timing of the contraction kernels, for benchmarks. While enabled (on != 0), each
  * tensor-core kernel launch is bracketed by two CUDA events recorded on its launch stream (the
  * library creates the events; it allocates no device memory). flce_timing_read() waits for the

@@ -161,3 +161,21 @@ def flce_backward(x: int, weight: int, target: int, lse: int, T: int, H: int, V:
     rc = lib().flce_backward(x, weight, target, lse, T, H, V, dtype, reduction, grad_loss,
                              grad_x, grad_weight, workspace, workspace_bytes, status, stream)
     return _check(rc, "flce_backward") if check else rc
+
+
+def flce_forward_static_scratch(x: int, weight: int, target: int, T: int, H: int, V: int,
+                                dtype: int, reduction: int, loss: int, lse: int, status: int,
+                                stream: int, check: bool = True) -> int:
+    """Enqueue the forward with the library's static device scratch (no workspace argument).
+
+    For callers that cannot allocate device memory; see include/flce.h for its size limit and
+    the sharing rules of the static scratch array.
+    """
+    L = lib()
+    fn = L.flce_forward_static_scratch
+    if fn.argtypes is None:
+        i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        fn.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, vp, vp, vp, vp]
+        fn.restype = ci
+    rc = fn(x, weight, target, T, H, V, dtype, reduction, loss, lse, status, stream)
+    return _check(rc, "flce_forward_static_scratch") if check else rc
