@@ -154,12 +154,33 @@ int flce_forward_static_scratch(const void* x, const void* weight, const int64_t
  * tensor-core kernel launch is bracketed by two CUDA events recorded on its launch stream (the
  * library creates the events; it allocates no device memory). flce_timing_read() waits for the
  * recorded events and returns, per kernel role, the number of launches and their summed
- * duration in milliseconds since the previous read, then forgets them. Roles (arrays of 4):
- *   0 forward projection + online log-sum-exp, 1 backward dz, 2 backward grad_weight,
- *   3 backward grad_x.
+ * duration in milliseconds since the previous read, then forgets them. Roles (arrays of
+ * FLCE_TIMING_ROLES): 0 forward projection + online log-sum-exp, 1 backward dz, 2 backward
+ * grad_weight alone and 3 backward grad_x alone (fp32 path), 4 backward grad_weight and grad_x
+ * of one vocab slab in a single launch (bf16 path).
  * Process-wide and not thread-safe. Returns FLCE_OK, FLCE_ERR_ARG or FLCE_ERR_CUDA. */
+#define FLCE_TIMING_ROLES 5
 int flce_timing_enable(int on);
-int flce_timing_read(int64_t counts[4], double ms[4]);
+int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_ROLES]);
+
+/* Process-wide tuning of the contraction kernels; results do not depend on these, only speed.
+ *   FLCE_TUNE_RASTER_ROWS  rows of a contraction's M dimension per raster group: tiles sweep
+ *                          the N dimension inside a group, so the group's A rows stay in L2
+ *                          while the B operand streams past. Multiple of 256; default 2048.
+ *   FLCE_TUNE_PAIR_GRADS   1: run the bf16 grad_weight and grad_x contractions of a vocab slab
+ *                          on pairs of SMs (tcgen05 cta_group::2, 256 x 256 tiles); 0: single-SM
+ *                          128 x 256 tiles; -1 (the default): pairs when every SM of the current
+ *                          device can be given a partner at once, single SMs otherwise (how many
+ *                          pairs fit depends on how a chip's SMs are grouped, not only on their
+ *                          number).
+ * Read at each launch. Returns FLCE_OK or FLCE_ERR_ARG. */
+#define FLCE_TUNE_RASTER_ROWS 1
+#define FLCE_TUNE_PAIR_GRADS 2
+int flce_set_tuning(int key, int64_t value);
+
+/* The value a tuning key takes on the current device (automatic choices resolved), in *value.
+ * Returns FLCE_OK, FLCE_ERR_ARG or FLCE_ERR_CUDA. */
+int flce_get_tuning(int key, int64_t* value);
 
 /* Static, human-readable name of a return code. Never NULL. */
 const char* flce_strerror(int code);

@@ -18,6 +18,7 @@ __all__ = [
     "flce_forward_workspace_size", "flce_backward_workspace_size", "flce_backward_slab_width",
     "flce_set_backward_slab_width", "flce_forward", "flce_backward", "flce_strerror",
     "flce_version", "flce_timing_enable", "flce_timing_read", "TIMING_ROLES",
+    "flce_set_tuning", "flce_get_tuning", "FLCE_TUNE_RASTER_ROWS", "FLCE_TUNE_PAIR_GRADS",
     "dtype_code", "reduction_code",
 ]
 
@@ -81,6 +82,10 @@ def lib() -> ctypes.CDLL:
     L.flce_timing_enable.restype = ci
     L.flce_timing_read.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
     L.flce_timing_read.restype = ci
+    L.flce_get_tuning.argtypes = [ci, ctypes.POINTER(i64)]
+    L.flce_get_tuning.restype = ci
+    L.flce_set_tuning.argtypes = [ci, i64]
+    L.flce_set_tuning.restype = ci
     L.flce_strerror.argtypes = [ci]
     L.flce_strerror.restype = ctypes.c_char_p
     L.flce_version.argtypes = []
@@ -128,7 +133,22 @@ def flce_set_backward_slab_width(vc: int) -> None:
     _check(int(lib().flce_set_backward_slab_width(int(vc))), "flce_set_backward_slab_width")
 
 
-TIMING_ROLES = ("forward", "backward_dz", "backward_grad_weight", "backward_grad_x")
+TIMING_ROLES = ("forward", "backward_dz", "backward_grad_weight", "backward_grad_x",
+                "backward_grads")
+FLCE_TUNE_RASTER_ROWS = 1
+FLCE_TUNE_PAIR_GRADS = 2
+
+
+def flce_get_tuning(key: int) -> int:
+    """Effective value of a tuning key on the current device (automatic choices resolved)."""
+    v = ctypes.c_int64()
+    _check(int(lib().flce_get_tuning(int(key), ctypes.byref(v))), "flce_get_tuning")
+    return int(v.value)
+
+
+def flce_set_tuning(key: int, value: int) -> None:
+    """Set a process-wide tuning value (FLCE_TUNE_*); affects speed only, never results."""
+    _check(int(lib().flce_set_tuning(int(key), int(value))), "flce_set_tuning")
 
 
 def flce_timing_enable(on: bool) -> None:
@@ -138,8 +158,8 @@ def flce_timing_enable(on: bool) -> None:
 
 def flce_timing_read() -> dict:
     """Launch counts and summed milliseconds per kernel role since the previous read."""
-    counts = (ctypes.c_int64 * 4)()
-    ms = (ctypes.c_double * 4)()
+    counts = (ctypes.c_int64 * len(TIMING_ROLES))()
+    ms = (ctypes.c_double * len(TIMING_ROLES))()
     _check(int(lib().flce_timing_read(counts, ms)), "flce_timing_read")
     return {r: (int(counts[i]), float(ms[i])) for i, r in enumerate(TIMING_ROLES)}
 

@@ -73,6 +73,16 @@ bool make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uin
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ------------------------------------------------------------------------------- tuning
+
+namespace {
+std::atomic<int> g_tune_raster_rows{2048};
+std::atomic<int> g_tune_pair_grads{-1};
+}  // namespace
+
+int tune_raster_rows() { return g_tune_raster_rows.load(); }
+int tune_pair_grads() { return g_tune_pair_grads.load(); }
+
 // ------------------------------------------------------------------------------- timing
 // Optional event brackets around each contraction launch (see flce_timing_enable).
 
@@ -295,14 +305,14 @@ int flce_timing_enable(int on) {
   return FLCE_OK;
 }
 
-int flce_timing_read(int64_t counts[4], double ms[4]) {
+int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_ROLES]) {
   if (!counts || !ms) return FLCE_ERR_ARG;
   std::vector<flce::TimedLaunch> done;
   {
     std::lock_guard<std::mutex> lock(flce::g_timing_mu);
     done.swap(flce::g_pending);
   }
-  for (int r = 0; r < 4; ++r) {
+  for (int r = 0; r < FLCE_TIMING_ROLES; ++r) {
     counts[r] = 0;
     ms[r] = 0.0;
   }
@@ -314,7 +324,7 @@ int flce_timing_read(int64_t counts[4], double ms[4]) {
       rc = FLCE_ERR_CUDA;
       continue;
     }
-    if (t.role >= 0 && t.role < 4) {
+    if (t.role >= 0 && t.role < FLCE_TIMING_ROLES) {
       counts[t.role] += 1;
       ms[t.role] += el;
     }
@@ -325,6 +335,38 @@ int flce_timing_read(int64_t counts[4], double ms[4]) {
     flce::g_event_pool.push_back(t.end);
   }
   return rc;
+}
+
+int flce_set_tuning(int key, int64_t value) {
+  switch (key) {
+    case FLCE_TUNE_RASTER_ROWS:
+      if (value < 256 || value > (int64_t(1) << 20) || value % 256 != 0) return FLCE_ERR_ARG;
+      flce::g_tune_raster_rows.store(static_cast<int>(value));
+      return FLCE_OK;
+    case FLCE_TUNE_PAIR_GRADS:
+      if (value < -1 || value > 1) return FLCE_ERR_ARG;
+      flce::g_tune_pair_grads.store(static_cast<int>(value));
+      return FLCE_OK;
+    default:
+      return FLCE_ERR_ARG;
+  }
+}
+
+int flce_get_tuning(int key, int64_t* value) {
+  if (!value) return FLCE_ERR_ARG;
+  switch (key) {
+    case FLCE_TUNE_RASTER_ROWS:
+      *value = flce::g_tune_raster_rows.load();
+      return FLCE_OK;
+    case FLCE_TUNE_PAIR_GRADS: {
+      flce::Device dev;
+      if (!flce::current_device(&dev)) return FLCE_ERR_CUDA;
+      *value = flce::use_pair_grads(dev.sms) ? 1 : 0;
+      return FLCE_OK;
+    }
+    default:
+      return FLCE_ERR_ARG;
+  }
 }
 
 int flce_set_backward_slab_width(int64_t vc) {
@@ -526,9 +568,8 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
         return FLCE_ERR_CUDA;
       e = flce::timed_launch(1, s, [&] { return flce::launch_dz_bf16(tx, tws, dz); });
       if (e == cudaSuccess)
-        e = flce::timed_launch(2, s, [&] { return flce::launch_gradw_bf16(tdz_mn, tx_mn, gw); });
-      if (e == cudaSuccess)
-        e = flce::timed_launch(3, s, [&] { return flce::launch_gradx_bf16(tdz_k, tw_mn, gx); });
+        e = flce::timed_launch(
+            4, s, [&] { return flce::launch_grads_bf16(tdz_mn, tx_mn, tdz_k, tw_mn, gw, gx); });
     } else {
       CUtensorMap twh, twl, tdzth, tdztl, tdzh, tdzl, twth, twtl;
       if (!flce::make_tmap_2d(&twh, DT, w.w_hi + size_t(slab0) * H, H, sw, H * 4, bk, kTileN) ||

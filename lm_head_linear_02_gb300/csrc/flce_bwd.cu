@@ -5,35 +5,27 @@
 // plus the TF32 hi/lo operand split used by the fp32 path.
 #include "epilogues.cuh"
 #include "flce_internal.h"
+#include "gemm_pair.cuh"
 
 namespace flce {
 
-template <bool kAMn, bool kBMn, bool kTF32, class Epi>
+// One problem M x N x K on the single-CTA core (operands K-major unless a_mn / b_mn).
+template <bool kTF32, class Epi>
 static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ta_lo,
                             const CUtensorMap& tb_lo, int M, int N, int K, int* status, int sms,
                             cudaStream_t stream, const typename Epi::Args& ea) {
-  using G = StageGeom<kTF32>;
-  auto kern = k_umma_gemm<kAMn, kBMn, kTF32, Epi>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  GemmGrid g;
-  g.m_tiles = (M + kBM - 1) / kBM;
-  g.n_tiles = (N + kBN - 1) / kBN;
-  g.k_blocks = (K + G::kBK - 1) / G::kBK;
-  g.group_m = kGroupM;
+  GemmGrid g{};
+  g.p[0] = make_problem(M, N, K, StageGeom<kTF32>::kBK, false, false, kBM, 0);
+  g.num_problems = 1;
   g.status = status;
-  const int tiles = g.m_tiles * g.n_tiles;
-  const int grid = tiles < sms ? tiles : sms;
-  kern<<<grid, kThreads, G::kSmemBytes, stream>>>(ta, tb, ta_lo, tb_lo, g, ea);
-  return cudaGetLastError();
+  return launch_gemm<kTF32, Epi, NoEpi>(ta, tb, ta_lo, tb_lo, g, ea, NoEpi::Args{}, sms, stream);
 }
 
 cudaError_t launch_dz_bf16(const CUtensorMap& tx, const CUtensorMap& tw_slab, const DzLaunch& p) {
   typename DzEpi<false>::Args ea{p.target, p.lse, p.dz, nullptr, nullptr, nullptr,
                                  p.ldz,    p.ldt, p.T,  p.slab0, p.slab_w};
-  return run_gemm<false, false, false, DzEpi<false>>(tx, tw_slab, tx, tw_slab, p.T, p.slab_w, p.H,
-                                                     p.status, p.sms, p.stream, ea);
+  return run_gemm<false, DzEpi<false>>(tx, tw_slab, tx, tw_slab, p.T, p.slab_w, p.H, p.status,
+                                       p.sms, p.stream, ea);
 }
 
 cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
@@ -49,38 +41,61 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
                                 p.T,
                                 p.slab0,
                                 p.slab_w};
-  return run_gemm<false, false, true, DzEpi<true>>(tx_hi, tw_hi, tx_lo, tw_lo, p.T, p.slab_w, p.H,
-                                                   p.status, p.sms, p.stream, ea);
+  return run_gemm<true, DzEpi<true>>(tx_hi, tw_hi, tx_lo, tw_lo, p.T, p.slab_w, p.H, p.status,
+                                     p.sms, p.stream, ea);
 }
 
-cudaError_t launch_gradw_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
-                              const GradWLaunch& p) {
-  typename GradWEpi<false>::Args ea{p.grad_w, p.grad_loss, p.scale, p.H, p.slab0, p.slab_w};
-  return run_gemm<true, true, false, GradWEpi<false>>(tdz_mn, tx_mn, tdz_mn, tx_mn, p.slab_w, p.H,
-                                                      p.T, p.status, p.sms, p.stream, ea);
+// grad_W (A = dz slab, B = x, both MN-major, K = T) and grad_x (A = dz slab K-major, B = W slab
+// MN-major, K = slab width) of one slab in a single launch: both read only the dz slab written
+// by the preceding dz launch, and one combined tile list fills the GPU evenly (two separate
+// launches of 2048 tiles each would leave the last of their 13.5 waves half empty).
+// Single-CTA 128 x 256 tiles by default; 256 x 256 tiles on CTA pairs with FLCE_TUNE_PAIR_GRADS.
+cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
+                              const CUtensorMap& tdz_k, const CUtensorMap& tw_mn,
+                              const GradWLaunch& pw, const GradXLaunch& px) {
+  typename GradWEpi<false>::Args ew{pw.grad_w, pw.grad_loss, pw.scale, pw.H, pw.slab0, pw.slab_w};
+  typename GradXEpi<false>::Args ex{px.acc,   px.grad_x, px.grad_loss, px.scale,
+                                    px.T,     px.H,      px.mode};
+  const bool pairs = use_pair_grads(pw.sms);
+  const int rows = pairs ? 256 : kBM;
+  GemmGrid g{};
+  g.p[0] = make_problem(pw.slab_w, pw.H, pw.T, 64, true, true, rows, 0);
+  g.p[1] = make_problem(px.T, px.H, px.K, 64, false, true, rows, g.p[0].m_tiles * g.p[0].n_tiles);
+  g.num_problems = 2;
+  g.status = pw.status;
+  if (pairs)
+    return launch_pair<GradWEpi<false>, GradXEpi<false>>(tdz_mn, tx_mn, tdz_k, tw_mn, g, ew, ex,
+                                                         pw.sms, pw.stream);
+  return launch_gemm<false, GradWEpi<false>, GradXEpi<false>>(tdz_mn, tx_mn, tdz_k, tw_mn, g, ew,
+                                                              ex, pw.sms, pw.stream);
+}
+
+bool use_pair_grads(int sms) {
+  const int t = tune_pair_grads();
+  if (t >= 0) return t != 0;
+  auto kern = k_umma_gemm_pair<GradWEpi<false>, GradXEpi<false>>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return 2 * pair_resident_clusters(kern, sms) >= 2 * (sms / 2);
 }
 
 cudaError_t launch_gradw_tf32(const CUtensorMap& tdzt_hi, const CUtensorMap& txt_hi,
                               const CUtensorMap& tdzt_lo, const CUtensorMap& txt_lo,
                               const GradWLaunch& p) {
   typename GradWEpi<true>::Args ea{p.grad_w, p.grad_loss, p.scale, p.H, p.slab0, p.slab_w};
-  return run_gemm<false, false, true, GradWEpi<true>>(tdzt_hi, txt_hi, tdzt_lo, txt_lo, p.slab_w,
-                                                      p.H, p.T, p.status, p.sms, p.stream, ea);
-}
-
-cudaError_t launch_gradx_bf16(const CUtensorMap& tdz_k, const CUtensorMap& tw_mn,
-                              const GradXLaunch& p) {
-  typename GradXEpi<false>::Args ea{p.acc, p.grad_x, p.grad_loss, p.scale, p.T, p.H, p.mode};
-  return run_gemm<false, true, false, GradXEpi<false>>(tdz_k, tw_mn, tdz_k, tw_mn, p.T, p.H, p.K,
-                                                       p.status, p.sms, p.stream, ea);
+  return run_gemm<true, GradWEpi<true>>(tdzt_hi, txt_hi, tdzt_lo, txt_lo, p.slab_w, p.H, p.T,
+                                        p.status, p.sms, p.stream, ea);
 }
 
 cudaError_t launch_gradx_tf32(const CUtensorMap& tdz_hi, const CUtensorMap& twt_hi,
                               const CUtensorMap& tdz_lo, const CUtensorMap& twt_lo,
                               const GradXLaunch& p) {
   typename GradXEpi<true>::Args ea{p.acc, p.grad_x, p.grad_loss, p.scale, p.T, p.H, p.mode};
-  return run_gemm<false, false, true, GradXEpi<true>>(tdz_hi, twt_hi, tdz_lo, twt_lo, p.T, p.H,
-                                                      p.K, p.status, p.sms, p.stream, ea);
+  return run_gemm<true, GradXEpi<true>>(tdz_hi, twt_hi, tdz_lo, twt_lo, p.T, p.H, p.K, p.status,
+                                        p.sms, p.stream, ea);
 }
 
 // ---------------------------------------------------------------------------- TF32 split

@@ -71,32 +71,25 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Projection + online log-sum-exp over all (token tile, vocab tile) pairs, then the combine
+// and finalize kernels.
 template <bool kTF32>
 static cudaError_t launch_forward(const CUtensorMap& tx, const CUtensorMap& tw,
                                   const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
                                   const FwdLaunch& p) {
-  using G = StageGeom<kTF32>;
-  auto kern = k_umma_gemm<false, false, kTF32, FwdEpi>;
-  // Per-device attribute; cheap enough to set on every call.
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  GemmGrid g;
-  g.m_tiles = (p.T + kBM - 1) / kBM;
-  g.n_tiles = (p.V + kBN - 1) / kBN;
-  g.k_blocks = (p.H + G::kBK - 1) / G::kBK;
-  g.group_m = kGroupM;
+  GemmGrid g{};
+  g.p[0] = make_problem(p.T, p.V, p.H, StageGeom<kTF32>::kBK, false, false, kBM, 0);
+  g.num_problems = 1;
   g.status = p.status;
   FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V};
-  const int tiles = g.m_tiles * g.n_tiles;
-  const int grid = tiles < p.sms ? tiles : p.sms;
-  kern<<<grid, kThreads, G::kSmemBytes, p.stream>>>(tx, tw, tx_lo, tw_lo, g, ea);
-  e = cudaGetLastError();
+  cudaError_t e = launch_gemm<kTF32, FwdEpi, NoEpi>(tx, tw, tx_lo, tw_lo, g, ea, NoEpi::Args{},
+                                                    p.sms, p.stream);
   if (e != cudaSuccess) return e;
 
+  const int n_tiles = (p.V + kBN - 1) / kBN;
   const int nblk = (p.T + kCombineThreads - 1) / kCombineThreads;
   k_fwd_combine<<<nblk, kCombineThreads, 0, p.stream>>>(p.part_m, p.part_s, p.zy, p.target, p.T,
-                                                        p.V, g.n_tiles, p.lse, p.block_sums,
+                                                        p.V, n_tiles, p.lse, p.block_sums,
                                                         p.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -14,8 +14,17 @@ namespace flce {
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 
-// Raster group (consecutive M tiles that walk N together) for L2 reuse of the B operand.
-constexpr int kGroupM = 16;
+// Process-wide tuning values (set through flce_set_tuning; read at each launch).
+//   tune_raster_rows(): rows of the M dimension per raster group (tiles walk N inside a group,
+//                       so the group's A rows stay in L2 while B streams); default 2048.
+//   tune_pair_grads():  run the two gradient contractions of a slab on CTA pairs (1), on single
+//                       CTAs (0), or decide per device (-1, the default: pairs when every SM
+//                       can be paired).
+int tune_raster_rows();
+int tune_pair_grads();
+
+// Whether the bf16 gradient launch of the current device runs on CTA pairs (resolves -1).
+bool use_pair_grads(int sms);
 
 struct Device {
   int id = -1;
@@ -79,9 +88,6 @@ struct GradWLaunch {
   int sms;
   cudaStream_t stream;
 };
-// bf16: A = dz slab (MN-major boxes {64 x 64}), B = x (MN-major boxes {64 x 64}).
-cudaError_t launch_gradw_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
-                              const GradWLaunch& p);
 // tf32: A = dz^T slab (K-major, hi/lo), B = x^T (K-major, hi/lo).
 cudaError_t launch_gradw_tf32(const CUtensorMap& tdzt_hi, const CUtensorMap& txt_hi,
                               const CUtensorMap& tdzt_lo, const CUtensorMap& txt_lo,
@@ -98,9 +104,12 @@ struct GradXLaunch {
   int sms;
   cudaStream_t stream;
 };
-// bf16: A = dz slab (K-major {64 x 128}), B = W slab (MN-major {64 x 64}).
-cudaError_t launch_gradx_bf16(const CUtensorMap& tdz_k, const CUtensorMap& tw_mn,
-                              const GradXLaunch& p);
+// bf16, one launch on CTA pairs (256 x 256 tiles) for both gradients of a slab:
+//   grad_W: A = dz slab (MN-major boxes {64 x 64}), B = x (MN-major boxes {64 x 64});
+//   grad_x: A = dz slab (K-major {64 x 128}), B = W slab (MN-major {64 x 64}).
+cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
+                              const CUtensorMap& tdz_k, const CUtensorMap& tw_mn,
+                              const GradWLaunch& pw, const GradXLaunch& px);
 // tf32: A = dz slab (K-major hi/lo), B = W^T slab (K-major hi/lo).
 cudaError_t launch_gradx_tf32(const CUtensorMap& tdz_hi, const CUtensorMap& twt_hi,
                               const CUtensorMap& tdz_lo, const CUtensorMap& twt_lo,

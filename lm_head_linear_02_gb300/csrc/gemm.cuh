@@ -17,6 +17,7 @@
 // each K-step issues hi.hi + hi.lo + lo.hi, which carries ~fp32 accuracy on TF32 tensor cores.
 #pragma once
 
+#include "flce_internal.h"
 #include "ptx.cuh"
 
 namespace flce {
@@ -27,22 +28,49 @@ constexpr int kThreads = 192;
 constexpr int kEpiWarp0 = 2;
 constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
 
-struct GemmGrid {
-  int m_tiles;   // ceil(M / 128)
-  int n_tiles;   // ceil(N / 256)
-  int k_blocks;  // ceil(K / BK)
-  int group_m;   // raster: tiles walk N inside groups of group_m consecutive M tiles
-  int* status;   // device status word (FLCE_STATUS_* bits)
+// One contraction D[M][N] = A . B^T of a launch. A launch carries one or two problems; their
+// tiles form one list (problem 0 first) that the persistent CTAs walk with a fixed stride.
+struct GemmProblem {
+  int m_tiles;     // ceil(M / tile rows)
+  int n_tiles;     // ceil(N / 256)
+  int k_blocks;    // ceil(K / BK)
+  int a_mn, b_mn;  // operand majors (1 = MN-major; bf16 only)
+  int group_m;     // raster: tiles walk N inside groups of group_m consecutive M tiles
+  int tile_begin;  // first linear tile of this problem within the launch
 };
 
-__device__ __forceinline__ void map_tile(const GemmGrid& g, int t, int& mb, int& nb) {
-  const int per_group = g.group_m * g.n_tiles;
-  const int grp = t / per_group;
-  const int first = grp * g.group_m;
-  const int gsz = min(g.group_m, g.m_tiles - first);
-  const int r = t - grp * per_group;
-  mb = first + r % gsz;
-  nb = r / gsz;
+struct GemmGrid {
+  GemmProblem p[2];
+  int num_problems;
+  int num_tiles;
+  int* status;  // device status word (FLCE_STATUS_* bits)
+};
+
+// The fields of the problem a tile belongs to, selected field by field (no dynamic indexing of
+// the parameter array, so everything stays in registers).
+struct TileInfo {
+  int prob, mb, nb, k_blocks, a_mn, b_mn;
+};
+
+__device__ __forceinline__ TileInfo map_tile(const GemmGrid& g, int t) {
+  const bool second = g.num_problems > 1 && t >= g.p[1].tile_begin;
+  const int m_tiles = second ? g.p[1].m_tiles : g.p[0].m_tiles;
+  const int n_tiles = second ? g.p[1].n_tiles : g.p[0].n_tiles;
+  const int group_m = second ? g.p[1].group_m : g.p[0].group_m;
+  const int r = t - (second ? g.p[1].tile_begin : g.p[0].tile_begin);
+  const int per_group = group_m * n_tiles;
+  const int grp = r / per_group;
+  const int first = grp * group_m;
+  const int gsz = min(group_m, m_tiles - first);
+  const int q = r - grp * per_group;
+  TileInfo ti;
+  ti.prob = second ? 1 : 0;
+  ti.mb = first + q % gsz;
+  ti.nb = q / gsz;
+  ti.k_blocks = second ? g.p[1].k_blocks : g.p[0].k_blocks;
+  ti.a_mn = second ? g.p[1].a_mn : g.p[0].a_mn;
+  ti.b_mn = second ? g.p[1].b_mn : g.p[0].b_mn;
+  return ti;
 }
 
 template <bool kTF32x3>
@@ -59,16 +87,22 @@ struct StageGeom {
   static constexpr uint32_t kSmemBytes = kRingBytes + 1024 + 1024;
 };
 
-// A stage holds [A_hi][A_lo][B_hi][B_lo] (lo copies only for kTF32x3).
-template <bool kAMn, bool kBMn, bool kTF32x3, class Epi>
+struct NoEpi {
+  struct Args {};
+  struct State {};
+  static __device__ __forceinline__ void init(const Args&, State&) {}
+  static __device__ __forceinline__ void tile(const Args&, State&, int, int, int, uint32_t) {}
+};
+
+// A stage holds [A_hi][A_lo][B_hi][B_lo] (lo copies only for kTF32x3, whose operands are
+// K-major and whose launches carry one problem: tA0/tB0 hold hi, tA1/tB1 hold lo).
+template <bool kTF32x3, class Epi0, class Epi1>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_umma_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmA_lo,
-                const __grid_constant__ CUtensorMap tmB_lo, const GemmGrid g,
-                const typename Epi::Args ea) {
+    k_umma_gemm(const __grid_constant__ CUtensorMap tA0, const __grid_constant__ CUtensorMap tB0,
+                const __grid_constant__ CUtensorMap tA1, const __grid_constant__ CUtensorMap tB1,
+                const GemmGrid g, const typename Epi0::Args e0, const typename Epi1::Args e1) {
   using G = StageGeom<kTF32x3>;
-  static_assert(!(kTF32x3 && (kAMn || kBMn)), "TF32 operands are K-major only");
-  constexpr uint32_t kIdesc = idesc_f32acc(kTF32x3 ? kFmtTF32 : kFmtBF16, kBM, kBN, kAMn, kBMn);
+  constexpr uint32_t kFmt = kTF32x3 ? kFmtTF32 : kFmtBF16;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -77,6 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // bars[0..S) full, [S..2S) empty, [2S..2S+2) tmem_full, [2S+2..2S+4) tmem_empty, [2S+4] drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::kStages + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // Pipeline counters kept in shared memory so that an aborted CTA can wait out its own
+  // copies and MMAs still in flight before it frees TMEM and exits.
+  int* issued_fills = reinterpret_cast<int*>(tmem_slot + 2);
+  int* consumed_fills = reinterpret_cast<int*>(tmem_slot + 3);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -86,12 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty_bar = [&](int s) { return bar0 + 8u * (G::kStages + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * G::kStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * G::kStages + 2 + a); };
-
   auto drain_bar = [&]() { return bar0 + 8u * (2 * G::kStages + 4); };
-  // Pipeline counters kept in shared memory so that an aborted CTA can wait out its own
-  // copies and MMAs still in flight before it frees TMEM and exits.
-  int* issued_fills = reinterpret_cast<int*>(tmem_slot + 2);
-  int* consumed_fills = reinterpret_cast<int*>(tmem_slot + 3);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::kStages; ++s) {
@@ -109,11 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch(&tmA);
-    tma_prefetch(&tmB);
-    if (kTF32x3) {
-      tma_prefetch(&tmA_lo);
-      tma_prefetch(&tmB_lo);
+    tma_prefetch(&tA0);
+    tma_prefetch(&tB0);
+    if (kTF32x3 || g.num_problems > 1) {
+      tma_prefetch(&tA1);
+      tma_prefetch(&tB1);
     }
   }
   if (warp == 1) {
@@ -125,8 +158,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_tiles = g.m_tiles * g.n_tiles;
-
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -134,11 +165,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int fills = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int mb, nb;
-        map_tile(g, t, mb, nb);
-        const int m0 = mb * kBM, n0 = nb * kBN;
-        for (int kb = 0; kb < g.k_blocks; ++kb) {
+      for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = map_tile(g, t);
+        const CUtensorMap* ta = (!kTF32x3 && ti.prob) ? &tA1 : &tA0;
+        const CUtensorMap* tb = (!kTF32x3 && ti.prob) ? &tB1 : &tB0;
+        const int m0 = ti.mb * kBM, n0 = ti.nb * kBN;
+        const bool a_mn = !kTF32x3 && ti.a_mn != 0;
+        const bool b_mn = !kTF32x3 && ti.b_mn != 0;
+        const int k_blocks = ti.k_blocks;
+        for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, g.status, abort_flag)) {
             ok = false;
             break;
@@ -148,19 +183,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sA = ring + stage * G::kStageBytes;
           const uint32_t sB = sA + G::kCopies * G::kABytes;
           const int k0 = kb * G::kBK;
-          if constexpr (!kAMn) {
-            tma_load_2d(sA, &tmA, fb, k0, m0);
-            if constexpr (kTF32x3) tma_load_2d(sA + G::kABytes, &tmA_lo, fb, k0, m0);
+          if (!a_mn) {
+            tma_load_2d(sA, ta, fb, k0, m0);
+            if constexpr (kTF32x3) tma_load_2d(sA + G::kABytes, &tA1, fb, k0, m0);
           } else {
 #pragma unroll
-            for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sA + j * 8192u, &tmA, fb, m0 + 64 * j, k0);
+            for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sA + j * 8192u, ta, fb, m0 + 64 * j, k0);
           }
-          if constexpr (!kBMn) {
-            tma_load_2d(sB, &tmB, fb, k0, n0);
-            if constexpr (kTF32x3) tma_load_2d(sB + G::kBBytes, &tmB_lo, fb, k0, n0);
+          if (!b_mn) {
+            tma_load_2d(sB, tb, fb, k0, n0);
+            if constexpr (kTF32x3) tma_load_2d(sB + G::kBBytes, &tB1, fb, k0, n0);
           } else {
 #pragma unroll
-            for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sB + j * 8192u, &tmB, fb, n0 + 64 * j, k0);
+            for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sB + j * 8192u, tb, fb, n0 + 64 * j, k0);
           }
           ++fills;
           if (++stage == G::kStages) {
@@ -181,34 +216,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       int consumed = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = map_tile(g, t);
+        const bool a_mn = !kTF32x3 && ti.a_mn != 0;
+        const bool b_mn = !kTF32x3 && ti.b_mn != 0;
+        const int k_blocks = ti.k_blocks;
+        const uint32_t idesc = idesc_f32acc(kFmt, kBM, kBN, a_mn, b_mn);
+        // Stage-0 descriptors and the per-K-step advance (16-byte units): K-major moves 32 B
+        // along the swizzled row, MN-major moves 16 bf16 K rows of 128 B.
+        const uint32_t sB0 = ring + G::kCopies * G::kABytes;
+        const uint64_t a_base =
+            a_mn ? sdesc_sw128(ring, 8192u, 1024u) : sdesc_sw128(ring, 16u, 1024u);
+        const uint64_t b_base =
+            b_mn ? sdesc_sw128(sB0, 8192u, 1024u) : sdesc_sw128(sB0, 16u, 1024u);
+        const uint64_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
+        const uint64_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, g.status, abort_flag)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        for (int kb = 0; kb < g.k_blocks; ++kb) {
+        for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, g.status, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t sA = ring + stage * G::kStageBytes;
-          const uint32_t sB = sA + G::kCopies * G::kABytes;
+          const uint64_t soff = static_cast<uint64_t>(stage * G::kStageBytes) >> 4;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            // K-major: advance 32 B along the swizzled row; MN-major: advance 16 (bf16) K rows.
-            const uint64_t a_hi = kAMn ? sdesc_sw128(sA + kk * 2048u, 8192u, 1024u)
-                                       : sdesc_sw128(sA + kk * 32u, 16u, 1024u);
-            const uint64_t b_hi = kBMn ? sdesc_sw128(sB + kk * 2048u, 8192u, 1024u)
-                                       : sdesc_sw128(sB + kk * 32u, 16u, 1024u);
+            const uint64_t a_hi = a_base + soff + kk * a_step;
+            const uint64_t b_hi = b_base + soff + kk * b_step;
             const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
             if constexpr (!kTF32x3) {
-              mma_bf16(d_tmem, a_hi, b_hi, kIdesc, accum);
+              mma_bf16(d_tmem, a_hi, b_hi, idesc, accum);
             } else {
-              const uint64_t a_lo = sdesc_sw128(sA + G::kABytes + kk * 32u, 16u, 1024u);
-              const uint64_t b_lo = sdesc_sw128(sB + G::kBBytes + kk * 32u, 16u, 1024u);
-              mma_tf32(d_tmem, a_lo, b_hi, kIdesc, accum);
-              mma_tf32(d_tmem, a_hi, b_lo, kIdesc, 1u);
-              mma_tf32(d_tmem, a_hi, b_hi, kIdesc, 1u);
+              const uint64_t a_lo = a_hi + (G::kABytes >> 4);
+              const uint64_t b_lo = b_hi + (G::kBBytes >> 4);
+              mma_tf32(d_tmem, a_lo, b_hi, idesc, accum);
+              mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
+              mma_tf32(d_tmem, a_hi, b_hi, idesc, 1u);
             }
           }
           mma_commit(empty_bar(stage));
@@ -234,17 +279,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    typename Epi::State st;
-    Epi::init(ea, st);
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    typename Epi0::State st0;
+    typename Epi1::State st1;
+    Epi0::init(e0, st0);
+    Epi1::init(e1, st1);
+    for (int t = blockIdx.x; t < g.num_tiles; t += gridDim.x) {
       if (!mbar_wait(tfull_bar(acc), acc_phase, g.status, abort_flag)) break;
       tc_fence_after_sync();
       __syncwarp();
-      int mb, nb;
-      map_tile(g, t, mb, nb);
+      const TileInfo ti = map_tile(g, t);
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      Epi::tile(ea, st, mb, nb, row, taddr);
+      if (ti.prob == 0)
+        Epi0::tile(e0, st0, ti.mb, ti.nb, row, taddr);
+      else
+        Epi1::tile(e1, st1, ti.mb, ti.nb, row, taddr);
       tc_fence_before_sync();
       mbar_arrive(tempty_bar(acc));
       if (++acc == 2) {
@@ -276,6 +325,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+// ---------------------------------------------------------------------------- host helpers
+
+// Problem description for a launch; `tile_rows` is 128 for this core, 256 for CTA pairs.
+inline GemmProblem make_problem(int M, int N, int K, int bk, bool a_mn, bool b_mn, int tile_rows,
+                                int tile_begin) {
+  GemmProblem p;
+  p.m_tiles = (M + tile_rows - 1) / tile_rows;
+  p.n_tiles = (N + kBN - 1) / kBN;
+  p.k_blocks = (K + bk - 1) / bk;
+  p.a_mn = a_mn ? 1 : 0;
+  p.b_mn = b_mn ? 1 : 0;
+  const int g = tune_raster_rows() / tile_rows;
+  p.group_m = g > 0 ? g : 1;
+  p.tile_begin = tile_begin;
+  return p;
+}
+
+inline void finish_grid(GemmGrid& g) {
+  g.num_tiles = 0;
+  for (int i = 0; i < g.num_problems; ++i)
+    g.num_tiles = g.p[i].tile_begin + g.p[i].m_tiles * g.p[i].n_tiles;
+}
+
+// Launch one or two problems on a persistent grid of single CTAs (one per SM, at most one
+// per tile).
+template <bool kTF32x3, class Epi0, class Epi1>
+cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
+                        const CUtensorMap& b1, GemmGrid g, const typename Epi0::Args& e0,
+                        const typename Epi1::Args& e1, int sms, cudaStream_t stream) {
+  using G = StageGeom<kTF32x3>;
+  auto kern = k_umma_gemm<kTF32x3, Epi0, Epi1>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  finish_grid(g);
+  const int grid = g.num_tiles < sms ? g.num_tiles : sms;
+  kern<<<grid, kThreads, G::kSmemBytes, stream>>>(a0, b0, a1, b1, g, e0, e1);
+  return cudaGetLastError();
 }
 
 }  // namespace flce

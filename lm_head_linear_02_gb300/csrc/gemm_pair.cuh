@@ -1,0 +1,306 @@
+// gemm_pair.cuh - the bf16 contraction core on CTA pairs (tcgen05 cta_group::2).
+//
+// A cluster of two CTAs on two SMs computes one 256 x 256 output tile with one MMA stream: CTA
+// r holds rows [128r, 128r + 128) of the A tile and rows [128r, 128r + 128) of the B tile (the
+// N dimension), the pair's tensor cores exchange the B halves, and CTA r's TMEM receives its 128
+// rows of D across all 256 columns. Per SM this halves the B operand that must be staged in
+// shared memory, so a 64-deep K slice costs 32 KB per CTA instead of 48 KB: six pipeline stages
+// fit where the single-CTA core holds four, and L2 -> SM traffic per FLOP drops by a third.
+//
+// Roles (6 warps per CTA, as in gemm.cuh):
+//   warp 0 (both CTAs)   TMA producer: loads this CTA's A and B halves; completion is counted
+//                        on the LEADER's full barrier, which the leader arms for both halves.
+//   warp 1 (leader)      MMA issuer: waits for both halves, issues M=256 N=256 MMAs, and
+//                        commits to the empty / tmem-full barriers of BOTH CTAs (multicast).
+//   warp 1 (peer)        idle (takes part in the pair's TMEM allocation only).
+//   warps 2..5 (both)    epilogue: drain this CTA's 128 accumulator rows, then tell the
+//                        leader (remote mbarrier arrive) that the accumulator is free.
+// A launch may carry two independent problems: grad_W and grad_x of one vocab slab run together,
+// so that their tiles fill the GPU in one wave pattern instead of two.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace flce {
+
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairABytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr uint32_t kPairBBytes = 128 * 128;  // this CTA's 128 N rows x 64 bf16
+constexpr uint32_t kPairStageBytes = kPairABytes + kPairBBytes;
+constexpr uint32_t kPairRingBytes = kPairStages * kPairStageBytes;
+constexpr uint32_t kPairSmemBytes = kPairRingBytes + 1024 + 1024;
+constexpr int kPairBK = 64;
+
+// Tiles are 256 x 256 here: GemmProblem::m_tiles counts 256-row tiles (make_problem with
+// tile_rows = 256) and the epilogue receives 128-row block indices (2 * mb + rank).
+template <class Epi0, class Epi1>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    k_umma_gemm_pair(const __grid_constant__ CUtensorMap tA0,
+                     const __grid_constant__ CUtensorMap tB0,
+                     const __grid_constant__ CUtensorMap tA1,
+                     const __grid_constant__ CUtensorMap tB1, const GemmGrid g,
+                     const typename Epi0::Args e0, const typename Epi1::Args e1) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairRingBytes);
+  // bars: [0,S) full, [S,2S) empty, [2S,2S+2) tmem_full, [2S+2,2S+4) tmem_empty, [2S+4] drain
+  uint32_t* slots = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5);
+  uint32_t* tmem_slot = slots;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
+  int* issued_fills = reinterpret_cast<int*>(slots + 2);
+  int* consumed_fills = reinterpret_cast<int*>(slots + 3);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kPairStages + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + 2 + a); };
+  auto drain_bar = [&]() { return bar0 + 8u * (2 * kPairStages + 4); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(full_bar(s), 1);   // leader: its own expect_tx arrive (+ both CTAs' bytes)
+      mbar_init(empty_bar(s), 1);  // one multicast commit from the leader's MMA thread
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);  // leader: 4 epilogue warps x 2 CTAs
+    }
+    mbar_init(drain_bar(), 1);
+    *abort_flag = 0;
+    *issued_fills = 0;
+    *consumed_fills = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tA0);
+    tma_prefetch(&tB0);
+    if (g.num_problems > 1) {
+      tma_prefetch(&tA1);
+      tma_prefetch(&tB1);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync_all();  // barrier inits and TMEM allocation visible to both CTAs
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int cluster_id = blockIdx.x >> 1;
+  const int n_clusters = gridDim.x >> 1;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int fills = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < g.num_tiles && ok; t += n_clusters) {
+        const TileInfo pt = map_tile(g, t);
+        const CUtensorMap* ta = pt.prob ? &tA1 : &tA0;
+        const CUtensorMap* tb = pt.prob ? &tB1 : &tB0;
+        const int m0 = pt.mb * 256 + static_cast<int>(rank) * 128;
+        const int n0 = pt.nb * 256 + static_cast<int>(rank) * 128;
+        const bool a_mn = pt.a_mn != 0, b_mn = pt.b_mn != 0;
+        const int k_blocks = pt.k_blocks;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, g.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
+          const uint32_t fb = mapa_shared(full_bar(stage), 0);
+          const uint32_t sA = ring + stage * kPairStageBytes;
+          const uint32_t sB = sA + kPairABytes;
+          const int k0 = kb * kPairBK;
+          if (!a_mn) {
+            tma_load_2d_pair(sA, ta, fb, k0, m0);
+          } else {
+            tma_load_2d_pair(sA, ta, fb, m0, k0);
+            tma_load_2d_pair(sA + 8192u, ta, fb, m0 + 64, k0);
+          }
+          if (!b_mn) {
+            tma_load_2d_pair(sB, tb, fb, k0, n0);
+          } else {
+            tma_load_2d_pair(sB, tb, fb, n0, k0);
+            tma_load_2d_pair(sB + 8192u, tb, fb, n0 + 64, k0);
+          }
+          ++fills;
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      *issued_fills = fills;
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (leader)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      int consumed = 0;
+      bool ok = true;
+      for (int t = cluster_id; t < g.num_tiles && ok; t += n_clusters) {
+        const TileInfo pt = map_tile(g, t);
+        const bool a_mn = pt.a_mn != 0, b_mn = pt.b_mn != 0;
+        const int k_blocks = pt.k_blocks;
+        const uint32_t idesc = idesc_f32acc(kFmtBF16, 256, 256, a_mn, b_mn);
+        // Descriptor of stage 0 and the per-K-step advance (in 16-byte units): K-major moves
+        // 32 B along the swizzled row, MN-major moves 16 K rows of 128 B.
+        const uint64_t a_base =
+            a_mn ? sdesc_sw128(ring, 8192u, 1024u) : sdesc_sw128(ring, 16u, 1024u);
+        const uint64_t b_base = b_mn ? sdesc_sw128(ring + kPairABytes, 8192u, 1024u)
+                                     : sdesc_sw128(ring + kPairABytes, 16u, 1024u);
+        const uint64_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
+        const uint64_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
+        // Accumulator handshake with both CTAs' epilogues: cluster-scope acquire.
+        if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, g.status, abort_flag)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, g.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint64_t soff = static_cast<uint64_t>(stage * kPairStageBytes) >> 4;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_pair(d_tmem, a_base + soff + kk * a_step, b_base + soff + kk * b_step, idesc,
+                          (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_pair(empty_bar(stage), 0x3);
+          ++consumed;
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair(tfull_bar(acc), 0x3);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      *consumed_fills = consumed;
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    typename Epi0::State st0;
+    typename Epi1::State st1;
+    Epi0::init(e0, st0);
+    Epi1::init(e1, st1);
+    for (int t = cluster_id; t < g.num_tiles; t += n_clusters) {
+      if (!mbar_wait(tfull_bar(acc), acc_phase, g.status, abort_flag)) break;
+      tc_fence_after_sync();
+      __syncwarp();
+      const TileInfo pt = map_tile(g, t);
+      const int mb128 = pt.mb * 2 + static_cast<int>(rank);
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * kBN) +
+                             (static_cast<uint32_t>(quarter * 32) << 16);
+      if (pt.prob == 0)
+        Epi0::tile(e0, st0, mb128, pt.nb, row, taddr);
+      else
+        Epi1::tile(e1, st1, mb128, pt.nb, row, taddr);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (*abort_flag) {
+    // A wait ran out of time somewhere in this CTA. Let in-flight work land before the pair's
+    // shared memory and TMEM go away: the leader drains its MMAs and waits for the fills it
+    // armed (they include the peer's bytes); the peer gives its own copies time to complete.
+    if (warp == 1 && lane == 0 && leader) {
+      mma_commit_pair(drain_bar(), 0x1);
+      mbar_wait_bounded(drain_bar(), 0u);
+    }
+    if (warp == 0 && lane == 0) {
+      if (leader) {
+        const int issued = *issued_fills;
+        for (int f = *consumed_fills; f < issued; ++f)
+          mbar_wait_bounded(full_bar(f % kPairStages),
+                            static_cast<uint32_t>((f / kPairStages) & 1));
+      } else {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) {
+        }
+      }
+    }
+    __syncwarp();
+    __syncthreads();
+  }
+  cluster_sync_all();  // no CTA leaves while its peer may still read its smem or signal it
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------- host helpers
+
+// How many CTA pairs of `kern` can be resident at once on the current device (queried once
+// per device and kernel). Depends on how the chip's SMs are grouped, not only on their count.
+template <class K>
+int pair_resident_clusters(K kern, int sms) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return sms / 2;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPairSmemBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // clear the query's error; fall back to one pair per two SMs
+    n = sms / 2;
+  }
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+// Launch one or two problems on CTA pairs: a persistent grid of as many pairs as can be
+// resident at once (at most one per tile).
+template <class Epi0, class Epi1>
+cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
+                        const CUtensorMap& b1, GemmGrid g, const typename Epi0::Args& e0,
+                        const typename Epi1::Args& e1, int sms, cudaStream_t stream) {
+  auto kern = k_umma_gemm_pair<Epi0, Epi1>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int max_clusters = pair_resident_clusters(kern, sms);
+  finish_grid(g);
+  const int clusters = g.num_tiles < max_clusters ? g.num_tiles : max_clusters;
+  kern<<<2 * clusters, kThreads, kPairSmemBytes, stream>>>(a0, b0, a1, b1, g, e0, e1);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

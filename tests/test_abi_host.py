@@ -155,3 +155,16 @@ def test_binding_raises_on_error(lib):
     with pytest.raises(B.FlceError) as e:
         B.flce_forward(0, 0, 0, 1, 8, 8, 0, 0, 0, 0, 0, 0, 0, 0)
     assert e.value.code == B.FLCE_ERR_ARG
+
+
+def test_tuning_knobs_validate(lib):
+    assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_ROWS) == 2048
+    for key, bad in [(B.FLCE_TUNE_RASTER_ROWS, 100), (B.FLCE_TUNE_RASTER_ROWS, 0),
+                     (B.FLCE_TUNE_PAIR_GRADS, 2), (B.FLCE_TUNE_PAIR_GRADS, -2), (99, 1)]:
+        with pytest.raises(B.FlceError):
+            B.flce_set_tuning(key, bad)
+    B.flce_set_tuning(B.FLCE_TUNE_RASTER_ROWS, 4096)
+    try:
+        assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_ROWS) == 4096
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_RASTER_ROWS, 2048)

@@ -111,6 +111,22 @@ def test_parity_multi_slab_backward(dtype, vc):
         B.flce_set_backward_slab_width(0)
 
 
+@pytest.mark.parametrize("pair", [0, 1])
+def test_parity_gradient_tiles_single_sm_and_sm_pairs(pair):
+    """Both tilings of the merged grad_W + grad_x launch, several slabs, ragged shapes."""
+    B.flce_set_tuning(B.FLCE_TUNE_PAIR_GRADS, pair)
+    B.flce_set_backward_slab_width(2048)
+    try:
+        assert B.flce_get_tuning(B.FLCE_TUNE_PAIR_GRADS) == pair
+        assert_full_parity(make_inputs("ragged", dtype="bf16"), "mean", grad_loss=1.25,
+                           label=f"ragged-bf16 pair={pair}")
+        assert_full_parity(make_inputs("tiny", T=300, H=264, V=700, dtype="bf16", seed=21), "sum",
+                           label=f"300x264x700 pair={pair}")
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_PAIR_GRADS, -1)
+        B.flce_set_backward_slab_width(0)
+
+
 @pytest.mark.parametrize("T,H,V,dtype", [
     (1, 64, 7, "bf16"),       # one token, vocab far below one tile
     (1, 8, 1, "f32"),         # V = 1: lse = z, loss 0, zero gradients
