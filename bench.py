@@ -16,6 +16,9 @@ workload's synthetic inputs, already resident in HBM. Prints ONE JSON line on ra
 * cpu_baseline: the float64 oracle timed on this host's cores on a bounded token sample.
 * --impl reference: the reference arm is the float64 oracle (there is no other implementation
   to run): each step is a bounded token sample of the same workload, timed on the host cores.
+* context.torch_eager: for comparison only, the unfused PyTorch formulation on the same GPU
+  (bf16 matmul through cuBLAS, logits upcast to fp32, cross_entropy, autograd backward), which
+  materialises the T x V logits; run when they fit comfortably in device memory.
 With N > 1 (torchrun) every rank runs an independent replica of the workload (weak scaling,
 no collective on the data path); the path has no exchange step.
 """
@@ -183,6 +186,42 @@ def workload_config(wl, n_slabs):
             "parallelism": "replicas"}
 
 
+# ------------------------------------------------------------------------------ context
+
+def torch_eager_context(x, w, y, steps: int = 3, warmup: int = 2):
+    """Time the materialised-logits PyTorch formulation of one fwd+bwd step (context only)."""
+    import torch
+
+    T, V = x.shape[0], w.shape[0]
+    need = T * V * (x.element_size() + 4 + 4 + 4)  # logits, fp32 copy, its grad, softmax
+    free, _ = torch.cuda.mem_get_info()
+    if need > 0.5 * free:
+        return {"skipped": f"logits need ~{need / 1e9:.1f} GB"}
+    xr = x.detach().clone().requires_grad_(True)
+    wr = w.detach().clone().requires_grad_(True)
+
+    def step():
+        loss = torch.nn.functional.cross_entropy((xr @ wr.T).float(), y, reduction="mean")
+        loss.backward()
+        xr.grad = None
+        wr.grad = None
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"torch_eager_ms_per_step": ms, "torch_eager_tokens_per_s": T / (ms * 1e-3),
+            "torch_eager_peak_mem_gb": torch.cuda.max_memory_allocated() / 1e9,
+            "what": "bf16 x @ W^T (cuBLAS), fp32 logits, F.cross_entropy, autograd backward"}
+
+
 # ------------------------------------------------------------------------------ our arm
 
 def cpu_baseline(inp, n_tokens: int):
@@ -338,14 +377,20 @@ def run_ours(args, wl, rank: int, world: int, dist):
     # both gradients (bf16), or dz, grad_W and grad_x plus 6 TF32 operand splits (fp32).
     launches_per_step = (3 + 2 * n_slabs) if wl.dtype == "bf16" else (9 + 3 * n_slabs)
     cpu = cpu_baseline(inp, args.oracle_tokens) if world == 1 else None
-    pair_grads = B.flce_get_tuning(B.FLCE_TUNE_PAIR_GRADS) if wl.dtype == "bf16" else 0
+    context = None
+    if world == 1 and not args.no_context:
+        del ws
+        torch.cuda.empty_cache()
+        context = {"torch_eager": torch_eager_context(x, w, y)}
+    pair_roles = B.flce_get_tuning(B.FLCE_TUNE_SM_PAIRS) if wl.dtype == "bf16" else 0
     out = {
         "metric": METRIC, "value": world * T * args.steps / (total_ms * 1e-3), "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic: seeded PCG64, x~N(0,1), weight~N(0,0.02^2), targets %s" % wl.target_dist,
         "config": dict(workload_config(wl, n_slabs),
-                       grad_tiles="256x256 on SM pairs" if pair_grads else "128x256 per SM"),
+                       sm_pair_roles=[n for n, b in (("forward", 1), ("dz", 2), ("grads", 4))
+                                      if pair_roles & b]),
         "fwd_ms": statistics.median(fwd_ms), "bwd_ms": statistics.median(bwd_ms),
         "fwd_tokens_per_s": T / (statistics.median(fwd_ms) * 1e-3),
         "tensor_tflops_step": step_tflops,
@@ -368,6 +413,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
         "peak_mem_gb": peak_mem / 1e9,
         "workspace_gb": max(fwd_ws, bwd_ws) / 1e9,
         "logits_bf16_gb": 2 * T * V / 1e9,
+        "context": context,
     }
     print(json.dumps(out), flush=True)
 
@@ -379,6 +425,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-context", action="store_true",
+                    help="skip the PyTorch eager context measurement")
     ap.add_argument("--oracle-tokens", type=int, default=64,
                     help="token sample per oracle step (CPU baseline / reference arm)")
     args = ap.parse_args()

@@ -72,9 +72,13 @@ extern "C" {
 #define FLCE_DTYPE_BF16 0
 #define FLCE_DTYPE_F32 1
 
-/* Reduction over tokens ("sum" and "mean", Liger-Kernel PR #928 failing-test list). */
+/* Reduction over tokens ("sum" and "mean", Liger-Kernel PR #928 failing-test list). NONE is an
+ * extension the pages do not list: the per-token losses l[t] = lse[t] - z[t, target[t]] that
+ * SUM and MEAN aggregate. With NONE, `loss` is float32[T] in flce_forward and `grad_loss` is
+ * float32[T] (one upstream gradient per token) in flce_backward. */
 #define FLCE_REDUCTION_SUM 0
 #define FLCE_REDUCTION_MEAN 1
+#define FLCE_REDUCTION_NONE 2
 
 /* Bytes of device workspace flce_forward needs for this problem; 0 for invalid arguments.
  * Holds per-(vocab tile, token) partial log-sum-exp terms, the target logits and per-block loss
@@ -100,7 +104,7 @@ int flce_set_backward_slab_width(int64_t vc);
  * Forward ("[example] fused_linear_cross_entropy kernel", Helion PR #1268, description of the
  * forward pass): computes loss[0] and the per-token log-sum-exp lse[T] that flce_backward needs.
  *   x [T][H], weight [V][H]  (dtype), target [T] int64   - inputs, device, read only
- *   loss [1] float32, lse [T] float32                     - outputs, device
+ *   loss [1] float32 ([T] for FLCE_REDUCTION_NONE), lse [T] float32 - outputs, device
  *   workspace: device, >= flce_forward_workspace_size() bytes, 256-byte aligned, scratch only
  *   status: device int, OR-ed with FLCE_STATUS_* bits
  *   stream: cudaStream_t to enqueue on
@@ -117,7 +121,7 @@ int flce_forward(const void* x, const void* weight, const int64_t* target,
  * vocab-slab schedule): recomputes the logits slab by slab, forms dz in registers and writes
  *   grad_x [T][H] = dz . weight   and   grad_weight [V][H] = dz^T . x     (dtype, device)
  * x, weight, target, lse: as passed to / produced by flce_forward (device, read only)
- * grad_loss [1] float32: device, the upstream gradient of loss
+ * grad_loss [1] float32 ([T] for FLCE_REDUCTION_NONE): device, the upstream gradient of loss
  * workspace: device, >= flce_backward_workspace_size() bytes, 256-byte aligned, scratch only
  * Returns FLCE_OK or a negative FLCE_ERR_* code.
  */
@@ -167,15 +171,18 @@ int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_RO
  *   FLCE_TUNE_RASTER_ROWS  rows of a contraction's M dimension per raster group: tiles sweep
  *                          the N dimension inside a group, so the group's A rows stay in L2
  *                          while the B operand streams past. Multiple of 256; default 2048.
- *   FLCE_TUNE_PAIR_GRADS   1: run the bf16 grad_weight and grad_x contractions of a vocab slab
- *                          on pairs of SMs (tcgen05 cta_group::2, 256 x 256 tiles); 0: single-SM
- *                          128 x 256 tiles; -1 (the default): pairs when every SM of the current
- *                          device can be given a partner at once, single SMs otherwise (how many
- *                          pairs fit depends on how a chip's SMs are grouped, not only on their
- *                          number).
+ *   FLCE_TUNE_SM_PAIRS     which bf16 contractions run on pairs of SMs (tcgen05 cta_group::2,
+ *                          256 x 256 tiles) instead of single-SM 128 x 256 tiles: a bit mask of
+ *                          FLCE_ROLE_FORWARD, FLCE_ROLE_DZ and FLCE_ROLE_GRADS; -1 (the default)
+ *                          picks a measured mask when every SM of the current device can be
+ *                          given a partner at once and 0 otherwise (how many pairs fit depends
+ *                          on how a chip's SMs are grouped, not only on their number).
  * Read at each launch. Returns FLCE_OK or FLCE_ERR_ARG. */
 #define FLCE_TUNE_RASTER_ROWS 1
-#define FLCE_TUNE_PAIR_GRADS 2
+#define FLCE_TUNE_SM_PAIRS 2
+#define FLCE_ROLE_FORWARD 1
+#define FLCE_ROLE_DZ 2
+#define FLCE_ROLE_GRADS 4
 int flce_set_tuning(int key, int64_t value);
 
 /* The value a tuning key takes on the current device (automatic choices resolved), in *value.

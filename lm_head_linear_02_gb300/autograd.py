@@ -55,12 +55,13 @@ def check_status(status: torch.Tensor) -> None:
 
 
 def flce_forward(x, weight, target, reduction: str = "mean", status: torch.Tensor | None = None):
-    """Enqueue the forward on the current stream. Returns (loss[1], lse[T], status[1])."""
+    """Enqueue the forward on the current stream. Returns (loss, lse[T], status[1]); loss has
+    one element, or T (the per-token losses) for reduction 'none'."""
     x, weight, target, T, H, V, dt = _prep(x, weight, target)
     dev = x.device
     ws_bytes = B.flce_forward_workspace_size(T, H, V, dt)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    loss = torch.empty(T if reduction == "none" else 1, dtype=torch.float32, device=dev)
     lse = torch.empty(T, dtype=torch.float32, device=dev)
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -72,11 +73,13 @@ def flce_forward(x, weight, target, reduction: str = "mean", status: torch.Tenso
 
 def flce_backward(x, weight, target, lse, grad_loss, reduction: str = "mean",
                   status: torch.Tensor | None = None):
-    """Enqueue the backward on the current stream. Returns (grad_x, grad_weight, status)."""
+    """Enqueue the backward on the current stream. Returns (grad_x, grad_weight, status).
+    grad_loss has one element, or one per token for reduction 'none'."""
     x, weight, target, T, H, V, dt = _prep(x, weight, target)
     dev = x.device
     lse = lse.to(torch.float32).contiguous()
-    grad_loss = grad_loss.reshape(1).to(device=dev, dtype=torch.float32).contiguous()
+    n = T if reduction == "none" else 1
+    grad_loss = grad_loss.reshape(n).to(device=dev, dtype=torch.float32).contiguous()
     ws_bytes = B.flce_backward_workspace_size(T, H, V, dt)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     grad_x = torch.empty_like(x)
@@ -98,7 +101,7 @@ class FLCEFunction(torch.autograd.Function):
         ctx.save_for_backward(x, weight, target, lse)
         ctx.reduction = reduction
         ctx.status = status
-        return loss.reshape(())
+        return loss if reduction == "none" else loss.reshape(())
 
     @staticmethod
     def backward(ctx, grad_loss):
@@ -109,5 +112,6 @@ class FLCEFunction(torch.autograd.Function):
 
 
 def flce(x, weight, target, reduction: str = "mean"):
-    """Fused linear cross-entropy loss (scalar, fp32) with autograd support."""
+    """Fused linear cross-entropy loss with autograd support: a scalar for 'sum' and 'mean',
+    the per-token losses [T] for 'none' (fp32)."""
     return FLCEFunction.apply(x, weight, target, reduction)

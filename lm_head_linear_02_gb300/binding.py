@@ -15,10 +15,11 @@ __all__ = [
     "FLCE_OK", "FLCE_ERR_ARG", "FLCE_ERR_UNSUPPORTED", "FLCE_ERR_WORKSPACE", "FLCE_ERR_ALIAS",
     "FLCE_ERR_CUDA", "FLCE_STATUS_TARGET_RANGE", "FLCE_STATUS_TIMEOUT",
     "FLCE_DTYPE_BF16", "FLCE_DTYPE_F32", "FLCE_REDUCTION_SUM", "FLCE_REDUCTION_MEAN",
+    "FLCE_REDUCTION_NONE",
     "flce_forward_workspace_size", "flce_backward_workspace_size", "flce_backward_slab_width",
     "flce_set_backward_slab_width", "flce_forward", "flce_backward", "flce_strerror",
     "flce_version", "flce_timing_enable", "flce_timing_read", "TIMING_ROLES",
-    "flce_set_tuning", "flce_get_tuning", "FLCE_TUNE_RASTER_ROWS", "FLCE_TUNE_PAIR_GRADS",
+    "flce_set_tuning", "flce_get_tuning", "FLCE_TUNE_RASTER_ROWS", "FLCE_TUNE_SM_PAIRS", "FLCE_ROLE_FORWARD", "FLCE_ROLE_DZ", "FLCE_ROLE_GRADS",
     "dtype_code", "reduction_code",
 ]
 
@@ -34,6 +35,7 @@ FLCE_DTYPE_BF16 = 0
 FLCE_DTYPE_F32 = 1
 FLCE_REDUCTION_SUM = 0
 FLCE_REDUCTION_MEAN = 1
+FLCE_REDUCTION_NONE = 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -99,7 +101,8 @@ def dtype_code(name: str) -> int:
 
 
 def reduction_code(name: str) -> int:
-    return {"sum": FLCE_REDUCTION_SUM, "mean": FLCE_REDUCTION_MEAN}[name]
+    return {"sum": FLCE_REDUCTION_SUM, "mean": FLCE_REDUCTION_MEAN,
+            "none": FLCE_REDUCTION_NONE}[name]
 
 
 def _check(rc: int, where: str) -> int:
@@ -136,7 +139,10 @@ def flce_set_backward_slab_width(vc: int) -> None:
 TIMING_ROLES = ("forward", "backward_dz", "backward_grad_weight", "backward_grad_x",
                 "backward_grads")
 FLCE_TUNE_RASTER_ROWS = 1
-FLCE_TUNE_PAIR_GRADS = 2
+FLCE_TUNE_SM_PAIRS = 2
+FLCE_ROLE_FORWARD = 1
+FLCE_ROLE_DZ = 2
+FLCE_ROLE_GRADS = 4
 
 
 def flce_get_tuning(key: int) -> int:

@@ -132,13 +132,16 @@ struct FwdEpi {
 // recomputed and turned into dz = (softmax - onehot(target)) * g in registers; here the
 // unscaled factor (softmax - onehot), whose entries lie in [-1, 1], is written to a bounded
 // vocab slab (T x Vc) that feeds the two gradient contractions, and g is applied in fp32 in
-// their epilogues. Keeping g out of the bf16 slab keeps the dominant -1 entries exact for any
-// reduction. Columns outside the slab are stored as 0; rows >= T are not stored.
+// their epilogues. Keeping g out of the bf16 slab keeps the dominant -1 entries exact for the
+// 'sum' and 'mean' reductions. With per-token upstream gradients ('none' reduction) each row is
+// multiplied by its own g[t] here instead (row_scale), since grad_W sums over the rows.
+// Columns outside the slab are stored as 0; rows >= T are not stored.
 template <bool kTF32>
 struct DzEpi {
   struct Args {
     const int64_t* target;
     const float* lse;
+    const float* row_scale;  // per-token upstream gradient [T], or null (factor 1)
     void* dz;      // bf16 [T][ldz] or fp32 hi [T][ldz]
     float* dz_lo;  // fp32 lo [T][ldz]          (tf32)
     float* dzt_hi; // fp32 [slab_w][ldt]        (tf32)
@@ -155,6 +158,7 @@ struct DzEpi {
     const bool valid = t < a.T;
     const float lsel = valid ? __ldg(a.lse + t) * kLog2e : 0.f;
     const long long y = valid ? static_cast<long long>(__ldg(a.target + t)) : -1ll;
+    const float rs = (valid && a.row_scale) ? __ldg(a.row_scale + t) : 1.0f;
     const int n0 = nb * kBN;  // slab-relative column of the tile
     const long long rel = y - a.slab0 - n0;
 #pragma unroll 1
@@ -168,7 +172,7 @@ struct DzEpi {
         float d = ex2(fmaf(v[j], kLog2e, -lsel));
         if (rel == c * 32 + j) d -= 1.0f;
         if (c0 + j >= a.slab_w) d = 0.f;
-        v[j] = d;
+        v[j] = d * rs;
       }
       if (!valid) continue;
       if constexpr (!kTF32) {
@@ -198,7 +202,8 @@ struct DzEpi {
 // grad_weight[slab rows, :] = dz_slab^T . x : the contraction runs over all T tokens, so each
 // output tile is complete when it leaves TMEM and is written exactly once.
 // The accumulator holds (softmax - onehot)^T . x; the gradient scale g = grad_loss (sum) or
-// grad_loss / T (mean) is applied here in fp32.
+// grad_loss / T (mean) is applied here in fp32 (grad_loss null: g = scale, the 'none' case whose
+// per-token factors are already in the dz rows).
 template <bool kF32Out>
 struct GradWEpi {
   struct Args {
@@ -211,7 +216,7 @@ struct GradWEpi {
     float g;
   };
   static __device__ __forceinline__ void init(const Args& a, State& st) {
-    st.g = __ldg(a.grad_loss) * a.scale;
+    st.g = a.grad_loss ? __ldg(a.grad_loss) * a.scale : a.scale;
   }
 
   static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
@@ -259,7 +264,7 @@ struct GradXEpi {
     float g;
   };
   static __device__ __forceinline__ void init(const Args& a, State& st) {
-    st.g = __ldg(a.grad_loss) * a.scale;
+    st.g = a.grad_loss ? __ldg(a.grad_loss) * a.scale : a.scale;
   }
 
   static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,

@@ -77,11 +77,11 @@ bool make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uin
 
 namespace {
 std::atomic<int> g_tune_raster_rows{2048};
-std::atomic<int> g_tune_pair_grads{-1};
+std::atomic<int> g_tune_sm_pairs{-1};
 }  // namespace
 
 int tune_raster_rows() { return g_tune_raster_rows.load(); }
-int tune_pair_grads() { return g_tune_pair_grads.load(); }
+int tune_sm_pairs() { return g_tune_sm_pairs.load(); }
 
 // ------------------------------------------------------------------------------- timing
 // Optional event brackets around each contraction launch (see flce_timing_enable).
@@ -343,9 +343,9 @@ int flce_set_tuning(int key, int64_t value) {
       if (value < 256 || value > (int64_t(1) << 20) || value % 256 != 0) return FLCE_ERR_ARG;
       flce::g_tune_raster_rows.store(static_cast<int>(value));
       return FLCE_OK;
-    case FLCE_TUNE_PAIR_GRADS:
-      if (value < -1 || value > 1) return FLCE_ERR_ARG;
-      flce::g_tune_pair_grads.store(static_cast<int>(value));
+    case FLCE_TUNE_SM_PAIRS:
+      if (value < -1 || value > 7) return FLCE_ERR_ARG;
+      flce::g_tune_sm_pairs.store(static_cast<int>(value));
       return FLCE_OK;
     default:
       return FLCE_ERR_ARG;
@@ -358,10 +358,10 @@ int flce_get_tuning(int key, int64_t* value) {
     case FLCE_TUNE_RASTER_ROWS:
       *value = flce::g_tune_raster_rows.load();
       return FLCE_OK;
-    case FLCE_TUNE_PAIR_GRADS: {
+    case FLCE_TUNE_SM_PAIRS: {
       flce::Device dev;
       if (!flce::current_device(&dev)) return FLCE_ERR_CUDA;
-      *value = flce::use_pair_grads(dev.sms) ? 1 : 0;
+      *value = flce::pair_roles(dev.sms);
       return FLCE_OK;
     }
     default:
@@ -381,7 +381,9 @@ int flce_forward(const void* x, const void* weight, const int64_t* target, int64
   // ---- host-side validation (no CUDA call before this block passes)
   if (!x || !weight || !target || !loss || !lse || !status) return FLCE_ERR_ARG;
   if (!dims_ok(T, H, V, dtype)) return FLCE_ERR_ARG;
-  if (reduction != FLCE_REDUCTION_SUM && reduction != FLCE_REDUCTION_MEAN) return FLCE_ERR_ARG;
+  if (reduction != FLCE_REDUCTION_SUM && reduction != FLCE_REDUCTION_MEAN &&
+      reduction != FLCE_REDUCTION_NONE)
+    return FLCE_ERR_ARG;
   const int eb = elem_bytes(dtype);
   if ((H * eb) % 16 != 0 || !aligned16(x) || !aligned16(weight)) return FLCE_ERR_UNSUPPORTED;
   const size_t need = flce_forward_workspace_size(T, H, V, dtype);
@@ -389,7 +391,8 @@ int flce_forward(const void* x, const void* weight, const int64_t* target, int64
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return FLCE_ERR_UNSUPPORTED;
   const Range in[3] = {rng(x, size_t(T) * H * eb), rng(weight, size_t(V) * H * eb),
                        rng(target, size_t(T) * 8)};
-  const Range out[4] = {rng(loss, 4), rng(lse, size_t(T) * 4), rng(workspace, need),
+  const size_t loss_bytes = reduction == FLCE_REDUCTION_NONE ? size_t(T) * 4 : 4;
+  const Range out[4] = {rng(loss, loss_bytes), rng(lse, size_t(T) * 4), rng(workspace, need),
                         rng(status, sizeof(int))};
   for (int i = 0; i < 4; ++i) {
     for (int j = 0; j < 3; ++j)
@@ -428,7 +431,8 @@ int flce_forward(const void* x, const void* weight, const int64_t* target, int64
   if (dtype == FLCE_DTYPE_BF16) {
     CUtensorMap tx, tw;
     if (!flce::make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, H, T, H * 2, 64, kTileM) ||
-        !flce::make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, weight, H, V, H * 2, 64, kTileN))
+        !flce::make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, weight, H, V, H * 2, 64,
+                            (flce::pair_roles(dev.sms) & FLCE_ROLE_FORWARD) ? 128 : kTileN))
       return FLCE_ERR_CUDA;
     e = flce::timed_launch(0, s, [&] { return flce::launch_forward_bf16(tx, tw, p); });
   } else {
@@ -456,7 +460,9 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
   if (!x || !weight || !target || !lse || !grad_loss || !grad_x || !grad_weight || !status)
     return FLCE_ERR_ARG;
   if (!dims_ok(T, H, V, dtype)) return FLCE_ERR_ARG;
-  if (reduction != FLCE_REDUCTION_SUM && reduction != FLCE_REDUCTION_MEAN) return FLCE_ERR_ARG;
+  if (reduction != FLCE_REDUCTION_SUM && reduction != FLCE_REDUCTION_MEAN &&
+      reduction != FLCE_REDUCTION_NONE)
+    return FLCE_ERR_ARG;
   const int eb = elem_bytes(dtype);
   if ((H * eb) % 16 != 0 || !aligned16(x) || !aligned16(weight) || !aligned16(grad_x) ||
       !aligned16(grad_weight))
@@ -465,7 +471,8 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
   if (!workspace || workspace_bytes < need) return FLCE_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return FLCE_ERR_UNSUPPORTED;
   const Range in[5] = {rng(x, size_t(T) * H * eb), rng(weight, size_t(V) * H * eb),
-                       rng(target, size_t(T) * 8), rng(lse, size_t(T) * 4), rng(grad_loss, 4)};
+                       rng(target, size_t(T) * 8), rng(lse, size_t(T) * 4),
+                       rng(grad_loss, reduction == FLCE_REDUCTION_NONE ? size_t(T) * 4 : 4)};
   const Range out[4] = {rng(grad_x, size_t(T) * H * eb), rng(grad_weight, size_t(V) * H * eb),
                         rng(workspace, need), rng(status, sizeof(int))};
   for (int i = 0; i < 4; ++i) {
@@ -519,6 +526,7 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
     flce::DzLaunch dz{};
     dz.target = target;
     dz.lse = lse;
+    dz.row_scale = reduction == FLCE_REDUCTION_NONE ? grad_loss : nullptr;
     dz.dz = w.dz;
     dz.dz_lo = w.dz_lo;
     dz.dzt_hi = w.dzt_hi;
@@ -535,7 +543,7 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
 
     flce::GradWLaunch gw{};
     gw.grad_w = grad_weight;
-    gw.grad_loss = grad_loss;
+    gw.grad_loss = reduction == FLCE_REDUCTION_NONE ? nullptr : grad_loss;
     gw.scale = scale;
     gw.H = int(H);
     gw.T = int(T);
@@ -548,7 +556,7 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
     flce::GradXLaunch gx{};
     gx.acc = bf16 ? w.acc : static_cast<float*>(grad_x);
     gx.grad_x = grad_x;
-    gx.grad_loss = grad_loss;
+    gx.grad_loss = reduction == FLCE_REDUCTION_NONE ? nullptr : grad_loss;
     gx.scale = scale;
     gx.mode = mode;
     gx.T = int(T);
@@ -561,7 +569,8 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
     if (bf16) {
       const uint8_t* wslab = static_cast<const uint8_t*>(weight) + size_t(slab0) * H * 2;
       CUtensorMap tws, tdz_mn, tdz_k, tw_mn;
-      if (!flce::make_tmap_2d(&tws, DT, wslab, H, sw, H * 2, bk, kTileN) ||
+      const uint32_t wbox = (flce::pair_roles(dev.sms) & FLCE_ROLE_DZ) ? 128 : kTileN;
+      if (!flce::make_tmap_2d(&tws, DT, wslab, H, sw, H * 2, bk, wbox) ||
           !flce::make_tmap_2d(&tdz_mn, DT, w.dz, sw, T, w.vc * 2, 64, 64) ||
           !flce::make_tmap_2d(&tdz_k, DT, w.dz, sw, T, w.vc * 2, bk, kTileM) ||
           !flce::make_tmap_2d(&tw_mn, DT, wslab, H, sw, H * 2, 64, 64))

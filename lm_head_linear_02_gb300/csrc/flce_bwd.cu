@@ -22,8 +22,16 @@ static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const 
 }
 
 cudaError_t launch_dz_bf16(const CUtensorMap& tx, const CUtensorMap& tw_slab, const DzLaunch& p) {
-  typename DzEpi<false>::Args ea{p.target, p.lse, p.dz, nullptr, nullptr, nullptr,
-                                 p.ldz,    p.ldt, p.T,  p.slab0, p.slab_w};
+  typename DzEpi<false>::Args ea{p.target, p.lse, p.row_scale, p.dz, nullptr, nullptr, nullptr,
+                                 p.ldz,    p.ldt, p.T,         p.slab0, p.slab_w};
+  if (pair_roles(p.sms) & FLCE_ROLE_DZ) {  // W slab map boxed {64 x 128} for this path
+    GemmGrid g{};
+    g.p[0] = make_problem(p.T, p.slab_w, p.H, 64, false, false, 256, 0);
+    g.num_problems = 1;
+    g.status = p.status;
+    return launch_pair<DzEpi<false>, NoEpi>(tx, tw_slab, tx, tw_slab, g, ea, NoEpi::Args{}, p.sms,
+                                            p.stream);
+  }
   return run_gemm<false, DzEpi<false>>(tx, tw_slab, tx, tw_slab, p.T, p.slab_w, p.H, p.status,
                                        p.sms, p.stream, ea);
 }
@@ -32,6 +40,7 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
                            const CUtensorMap& tx_lo, const CUtensorMap& tw_lo, const DzLaunch& p) {
   typename DzEpi<true>::Args ea{p.target,
                                 p.lse,
+                                p.row_scale,
                                 p.dz,
                                 static_cast<float*>(p.dz_lo),
                                 static_cast<float*>(p.dzt_hi),
@@ -49,14 +58,14 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
 // MN-major, K = slab width) of one slab in a single launch: both read only the dz slab written
 // by the preceding dz launch, and one combined tile list fills the GPU evenly (two separate
 // launches of 2048 tiles each would leave the last of their 13.5 waves half empty).
-// Single-CTA 128 x 256 tiles by default; 256 x 256 tiles on CTA pairs with FLCE_TUNE_PAIR_GRADS.
+// Single-CTA 128 x 256 tiles, or 256 x 256 tiles on CTA pairs (FLCE_ROLE_GRADS in the pair mask).
 cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
                               const CUtensorMap& tdz_k, const CUtensorMap& tw_mn,
                               const GradWLaunch& pw, const GradXLaunch& px) {
   typename GradWEpi<false>::Args ew{pw.grad_w, pw.grad_loss, pw.scale, pw.H, pw.slab0, pw.slab_w};
   typename GradXEpi<false>::Args ex{px.acc,   px.grad_x, px.grad_loss, px.scale,
                                     px.T,     px.H,      px.mode};
-  const bool pairs = use_pair_grads(pw.sms);
+  const bool pairs = (pair_roles(pw.sms) & FLCE_ROLE_GRADS) != 0;
   const int rows = pairs ? 256 : kBM;
   GemmGrid g{};
   g.p[0] = make_problem(pw.slab_w, pw.H, pw.T, 64, true, true, rows, 0);
@@ -70,16 +79,16 @@ cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
                                                               ex, pw.sms, pw.stream);
 }
 
-bool use_pair_grads(int sms) {
-  const int t = tune_pair_grads();
-  if (t >= 0) return t != 0;
+int pair_roles(int sms) {
+  const int t = tune_sm_pairs();
+  if (t >= 0) return t;
   auto kern = k_umma_gemm_pair<GradWEpi<false>, GradXEpi<false>>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) !=
       cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return 0;
   }
-  return 2 * pair_resident_clusters(kern, sms) >= 2 * (sms / 2);
+  return 2 * pair_resident_clusters(kern, sms) >= 2 * (sms / 2) ? kAutoPairRoles : 0;
 }
 
 cudaError_t launch_gradw_tf32(const CUtensorMap& tdzt_hi, const CUtensorMap& txt_hi,

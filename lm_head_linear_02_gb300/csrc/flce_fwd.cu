@@ -3,6 +3,7 @@
 // reduction.
 #include "epilogues.cuh"
 #include "flce_internal.h"
+#include "gemm_pair.cuh"
 
 namespace flce {
 
@@ -10,12 +11,13 @@ constexpr int kCombineThreads = 256;
 
 // Merge the per-(vocab tile) partials of each token in increasing tile order:
 //   M = max_i m_i,  S = sum_i s_i exp(m_i - M),  lse = M + ln S,  l = lse - z[t, target[t]].
-// Writes lse[t] and one partial loss sum per block (fixed-order tree).
+// Writes lse[t] and one partial loss sum per block (fixed-order tree); with per_token non-null
+// (the 'none' reduction) it also writes l[t] there.
 __global__ void __launch_bounds__(kCombineThreads)
     k_fwd_combine(const float* __restrict__ part_m, const float* __restrict__ part_s,
                   const float* __restrict__ zy, const int64_t* __restrict__ target, int T, int V,
                   int n_tiles, float* __restrict__ lse, float* __restrict__ block_sums,
-                  int* status) {
+                  float* __restrict__ per_token, int* status) {
   const int t = blockIdx.x * kCombineThreads + threadIdx.x;
   float l = 0.f;
   if (t < T) {
@@ -36,6 +38,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     } else {
       l = lse_t - zy[t];
     }
+    if (per_token) per_token[t] = l;
   }
   // Fixed-order block reduction: shuffle tree within each warp, then over the warp sums.
   __shared__ float warp_sums[kCombineThreads / 32];
@@ -71,6 +74,8 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+static cudaError_t launch_combine(const FwdLaunch& p);
+
 // Projection + online log-sum-exp over all (token tile, vocab tile) pairs, then the combine
 // and finalize kernels.
 template <bool kTF32>
@@ -85,19 +90,36 @@ static cudaError_t launch_forward(const CUtensorMap& tx, const CUtensorMap& tw,
   cudaError_t e = launch_gemm<kTF32, FwdEpi, NoEpi>(tx, tw, tx_lo, tw_lo, g, ea, NoEpi::Args{},
                                                     p.sms, p.stream);
   if (e != cudaSuccess) return e;
+  return launch_combine(p);
+}
 
+// The combine (lse, per-token loss, block sums) and finalize kernels after the projection.
+static cudaError_t launch_combine(const FwdLaunch& p) {
+  cudaError_t e;
   const int n_tiles = (p.V + kBN - 1) / kBN;
   const int nblk = (p.T + kCombineThreads - 1) / kCombineThreads;
+  const bool none = p.reduction == FLCE_REDUCTION_NONE;
   k_fwd_combine<<<nblk, kCombineThreads, 0, p.stream>>>(p.part_m, p.part_s, p.zy, p.target, p.T,
                                                         p.V, n_tiles, p.lse, p.block_sums,
-                                                        p.status);
+                                                        none ? p.loss : nullptr, p.status);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || none) return e;
   k_fwd_finalize<<<1, 256, 0, p.stream>>>(p.block_sums, nblk, p.T, p.reduction, p.loss);
   return cudaGetLastError();
 }
 
 cudaError_t launch_forward_bf16(const CUtensorMap& tx, const CUtensorMap& tw, const FwdLaunch& p) {
+  if (pair_roles(p.sms) & FLCE_ROLE_FORWARD) {  // W map boxed {64 x 128} for this path
+    GemmGrid g{};
+    g.p[0] = make_problem(p.T, p.V, p.H, 64, false, false, 256, 0);
+    g.num_problems = 1;
+    g.status = p.status;
+    FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V};
+    cudaError_t e = launch_pair<FwdEpi, NoEpi>(tx, tw, tx, tw, g, ea, NoEpi::Args{}, p.sms,
+                                               p.stream);
+    if (e != cudaSuccess) return e;
+    return launch_combine(p);
+  }
   return launch_forward<false>(tx, tw, tx, tw, p);
 }
 

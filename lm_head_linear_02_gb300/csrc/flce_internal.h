@@ -17,14 +17,17 @@ constexpr int kTileN = 256;
 // Process-wide tuning values (set through flce_set_tuning; read at each launch).
 //   tune_raster_rows(): rows of the M dimension per raster group (tiles walk N inside a group,
 //                       so the group's A rows stay in L2 while B streams); default 2048.
-//   tune_pair_grads():  run the two gradient contractions of a slab on CTA pairs (1), on single
-//                       CTAs (0), or decide per device (-1, the default: pairs when every SM
-//                       can be paired).
+//   tune_sm_pairs():    bit mask of the bf16 roles (FLCE_ROLE_*) that run on CTA pairs, or -1
+//                       (the default) to decide per device.
 int tune_raster_rows();
-int tune_pair_grads();
+int tune_sm_pairs();
 
-// Whether the bf16 gradient launch of the current device runs on CTA pairs (resolves -1).
-bool use_pair_grads(int sms);
+// Roles measured faster on CTA pairs, used by the automatic choice when every SM of the device
+// can be paired.
+constexpr int kAutoPairRoles = FLCE_ROLE_GRADS;
+
+// Effective FLCE_ROLE_* mask of bf16 roles that run on CTA pairs on the current device.
+int pair_roles(int sms);
 
 struct Device {
   int id = -1;
@@ -49,7 +52,7 @@ struct FwdLaunch {
   float* zy;          // [T]
   float* block_sums;  // [ceil(T / 256)]
   float* lse;         // [T]
-  float* loss;        // [1]
+  float* loss;        // [1], or [T] for the 'none' reduction
   int* status;
   int T, H, V, reduction;
   int sms;
@@ -65,6 +68,7 @@ cudaError_t launch_forward_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_
 struct DzLaunch {
   const int64_t* target;
   const float* lse;
+  const float* row_scale;  // per-token upstream gradient ('none' reduction) or null
   void* dz;           // (softmax - onehot): bf16 [T][ldz] or fp32 hi [T][ldz]
   void* dz_lo;        // fp32 lo [T][ldz] (tf32 path)
   void* dzt_hi;       // fp32 [Vc][ldt] transposed hi (tf32 path)
@@ -81,8 +85,8 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
 
 struct GradWLaunch {
   void* grad_w;  // [V][H] (dtype); rows slab0 .. slab0 + slab_w are written
-  const float* grad_loss;
-  float scale;   // 1 (sum) or 1/T (mean); g = grad_loss[0] * scale
+  const float* grad_loss;  // null for the 'none' reduction (g = scale = 1)
+  float scale;   // 1 (sum, none) or 1/T (mean); g = grad_loss[0] * scale
   int H, T, slab0, slab_w;
   int* status;
   int sms;

@@ -10,7 +10,9 @@ Workloads are the LM-head shapes of the pages' benchmarks:
 * "Fused linear + cross-entropy" (KernelIndex operation page), "Current records": vocab 128256,
   hidden 4096, tokens in {4096, 8192, 16384, 32768}, bf16.
 * "feat(FLCE): add helion version of fused linear cross entropy" (Liger-Kernel PR #928), the
-  failing-test list: (B, T, H, V) = (2, 1024, 4096, 32000) and (3, 423, 1000, 10000).
+  failing-test list: (B, T, H, V) = (2, 1024, 4096, 32000) and (3, 423, 1000, 10000); and its
+  benchmark tables for a Qwen3 head (H=4096, V=151936, BT=32768) and a Gemma3 head (H=2304,
+  V=262208, BT=8192).
 
 The pages ship no datasets; these synthetic draws stand in for the benchmark scripts' random
 activations and weights: x ~ N(0, 1), weight ~ N(0, 0.02^2), and targets either uniform over the
@@ -74,6 +76,10 @@ WORKLOADS = {
                  note="headline workload"),
         Workload("llama3_head_t32768", 5, 32768, 4096, 128256, "bf16", "uniform", ("mean",),
                  note="large batch; peak memory must stay below the bf16 logits size"),
+        Workload("qwen3_head_t32768", 6, 32768, 4096, 151936, "bf16", "uniform", ("mean",),
+                 note="Qwen3-sized head"),
+        Workload("gemma3_head_t8192", 7, 8192, 2304, 262208, "bf16", "uniform", ("mean",),
+                 note="Gemma3-sized head: narrow hidden, very wide vocabulary"),
     ]
 }
 

@@ -24,8 +24,8 @@ the definition written out in float64:
     z[t, v]   = sum_h x[t, h] * weight[v, h]
     lse[t]    = m_t + ln sum_v exp(z[t, v] - m_t),      m_t = max_v z[t, v]
     l[t]      = lse[t] - z[t, target[t]]
-    loss      = sum_t l[t]            (sum)   or   (1/T) sum_t l[t]   (mean)
-    g         = grad_loss             (sum)   or   grad_loss / T      (mean)
+    loss      = sum_t l[t]            (sum)   or   (1/T) sum_t l[t]   (mean)   or   l   (none)
+    g         = grad_loss             (sum)   or   grad_loss / T      (mean)   or   grad_loss[t]
     dz[t, v]  = (exp(z[t, v] - lse[t]) - [v == target[t]]) * g
     grad_x    = dz . weight          grad_weight = dz^T . x
 
@@ -34,7 +34,9 @@ the same formulas, and grad_weight is summed over chunks in increasing token ord
 
 Readings where the pages are silent: no bias term; natural logarithm; the 'mean' denominator is
 the token count T (the pages define no ignore_index, so every target counts and a target outside
-[0, V) is an error); loss is a scalar.
+[0, V) is an error); loss is a scalar for 'sum' and 'mean'. The 'none' reduction (an extension:
+the pages list only 'sum' and 'mean') returns the per-token losses l[t] that the two reductions
+aggregate, and its backward takes one upstream gradient per token.
 
 Pins (tests/test_oracle_pins.py): closed forms for weight = 0, x = 0 and identical weight rows,
 a hand-derived 2x2x3 example (tests/golden/), brute-force pure-Python loops, torch's float64
@@ -57,7 +59,7 @@ __all__ = [
     "sampled_rows",
 ]
 
-REDUCTIONS = ("sum", "mean")
+REDUCTIONS = ("sum", "mean", "none")
 
 
 def _check(x, weight, target):
@@ -85,20 +87,28 @@ def log_sum_exp(z: np.ndarray) -> np.ndarray:
     return m + np.log(np.exp(z - m[:, None]).sum(axis=1))
 
 
-def grad_scale(grad_loss: float, reduction: str, T: int) -> float:
-    """g: d loss / d l[t] times the incoming grad_loss ('sum' -> 1, 'mean' -> 1/T)."""
+def grad_scale(grad_loss, reduction: str, T: int):
+    """g: d loss / d l[t] times the incoming grad_loss ('sum' -> 1, 'mean' -> 1/T, 'none' -> the
+    per-token upstream gradients themselves, an array of T values)."""
     if reduction == "sum":
         return float(grad_loss)
     if reduction == "mean":
         return float(grad_loss) / T
+    if reduction == "none":
+        g = np.asarray(grad_loss, dtype=np.float64).reshape(-1)
+        if g.shape != (T,):
+            raise ValueError("reduction 'none' needs one upstream gradient per token")
+        return g
     raise ValueError(f"reduction must be one of {REDUCTIONS}")
 
 
-def dlogits(z: np.ndarray, lse: np.ndarray, target: np.ndarray, g: float) -> np.ndarray:
-    """dz = (softmax(z) - onehot(target)) * g for a block of rows (Helion PR #1268, backward)."""
+def dlogits(z: np.ndarray, lse: np.ndarray, target: np.ndarray, g) -> np.ndarray:
+    """dz = (softmax(z) - onehot(target)) * g for a block of rows (Helion PR #1268, backward);
+    g is a scalar or one value per row."""
     p = np.exp(z - lse[:, None])
     p[np.arange(z.shape[0]), target] -= 1.0
-    return p * g
+    g = np.asarray(g, dtype=np.float64)
+    return p * (g[:, None] if g.ndim == 1 else g)
 
 
 def forward(x, weight, target, reduction: str = "mean", chunk: int = 256):
@@ -114,12 +124,14 @@ def forward(x, weight, target, reduction: str = "mean", chunk: int = 256):
         z = logits(x[t0:t1], weight)
         lse[t0:t1] = log_sum_exp(z)
         per_token[t0:t1] = lse[t0:t1] - z[np.arange(t1 - t0), target[t0:t1]]
+    if reduction == "none":
+        return per_token, lse
     total = per_token.sum()
     loss = total if reduction == "sum" else total / T
     return float(loss), lse
 
 
-def backward(x, weight, target, lse, reduction: str = "mean", grad_loss: float = 1.0,
+def backward(x, weight, target, lse, reduction: str = "mean", grad_loss=1.0,
              chunk: int = 256):
     """grad_x and grad_weight from recomputed logits (Helion PR #1268, backward)."""
     x, weight, target = _check(x, weight, target)
@@ -131,20 +143,22 @@ def backward(x, weight, target, lse, reduction: str = "mean", grad_loss: float =
     for t0 in range(0, T, chunk):
         t1 = min(T, t0 + chunk)
         z = logits(x[t0:t1], weight)
-        dz = dlogits(z, lse[t0:t1], target[t0:t1], g)
+        gc = g[t0:t1] if isinstance(g, np.ndarray) else g
+        dz = dlogits(z, lse[t0:t1], target[t0:t1], gc)
         grad_x[t0:t1] = dz @ weight
         grad_w += dz.T @ x[t0:t1]
     return grad_x, grad_w
 
 
-def flce(x, weight, target, reduction: str = "mean", grad_loss: float = 1.0, chunk: int = 256):
-    """Forward and backward in one call: dict with loss, lse, grad_x, grad_weight (float64)."""
+def flce(x, weight, target, reduction: str = "mean", grad_loss=1.0, chunk: int = 256):
+    """Forward and backward in one call: dict with loss, lse, grad_x, grad_weight (float64).
+    For 'none' the loss is the per-token array and grad_loss holds one value per token."""
     loss, lse = forward(x, weight, target, reduction, chunk)
     grad_x, grad_w = backward(x, weight, target, lse, reduction, grad_loss, chunk)
     return {"loss": loss, "lse": lse, "grad_x": grad_x, "grad_weight": grad_w}
 
 
-def sampled_rows(x, weight, target, rows, reduction: str = "mean", grad_loss: float = 1.0):
+def sampled_rows(x, weight, target, rows, reduction: str = "mean", grad_loss=1.0):
     """lse, per-token loss and grad_x for selected token rows only.
 
     Each token row depends on its own logits row alone, so these values are exact for any total
@@ -154,6 +168,8 @@ def sampled_rows(x, weight, target, rows, reduction: str = "mean", grad_loss: fl
     T = np.asarray(x).shape[0]
     x_rows, weight, target_rows = _check(np.asarray(x)[rows], weight, np.asarray(target)[rows])
     g = grad_scale(grad_loss, reduction, T)
+    if isinstance(g, np.ndarray):
+        g = g[rows]
     z = logits(x_rows, weight)
     lse = log_sum_exp(z)
     per_token = lse - z[np.arange(rows.size), target_rows]

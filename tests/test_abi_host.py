@@ -121,7 +121,7 @@ def _bwd(**kw):
     (dict(V=-3), B.FLCE_ERR_ARG),
     (dict(T=1 << 30), B.FLCE_ERR_ARG),
     (dict(dtype=2), B.FLCE_ERR_ARG),
-    (dict(reduction=2), B.FLCE_ERR_ARG),
+    (dict(reduction=3), B.FLCE_ERR_ARG),
     (dict(H=60), B.FLCE_ERR_UNSUPPORTED),          # 120-byte rows for bf16
     (dict(H=6, dtype=1), B.FLCE_ERR_UNSUPPORTED),  # 24-byte rows for f32
     (dict(x=FAKE + 8), B.FLCE_ERR_UNSUPPORTED),
@@ -160,7 +160,7 @@ def test_binding_raises_on_error(lib):
 def test_tuning_knobs_validate(lib):
     assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_ROWS) == 2048
     for key, bad in [(B.FLCE_TUNE_RASTER_ROWS, 100), (B.FLCE_TUNE_RASTER_ROWS, 0),
-                     (B.FLCE_TUNE_PAIR_GRADS, 2), (B.FLCE_TUNE_PAIR_GRADS, -2), (99, 1)]:
+                     (B.FLCE_TUNE_SM_PAIRS, 8), (B.FLCE_TUNE_SM_PAIRS, -2), (99, 1)]:
         with pytest.raises(B.FlceError):
             B.flce_set_tuning(key, bad)
     B.flce_set_tuning(B.FLCE_TUNE_RASTER_ROWS, 4096)

@@ -111,19 +111,42 @@ def test_parity_multi_slab_backward(dtype, vc):
         B.flce_set_backward_slab_width(0)
 
 
-@pytest.mark.parametrize("pair", [0, 1])
-def test_parity_gradient_tiles_single_sm_and_sm_pairs(pair):
-    """Both tilings of the merged grad_W + grad_x launch, several slabs, ragged shapes."""
-    B.flce_set_tuning(B.FLCE_TUNE_PAIR_GRADS, pair)
+@pytest.mark.parametrize("name,dtype", [("ragged", "f32"), ("ragged", "bf16"), ("llama2_head", "bf16")])
+def test_parity_reduction_none(name, dtype):
+    """Per-token losses and gradients under a random per-token upstream gradient."""
+    inp = make_inputs(name, dtype=dtype)
+    T = inp.workload.T
+    u = np.random.default_rng(T).standard_normal(T).astype(np.float32)
+    x, w, y = to_device(inp)
+    loss, lse, status = A.flce_forward(x, w, y, "none")
+    gx, gw, status = A.flce_backward(x, w, y, lse, torch.from_numpy(u).cuda(), "none",
+                                     status=status)
+    torch.cuda.synchronize()
+    A.check_status(status)
+    ref = oracle.flce(inp.x, inp.weight, inp.target, "none", grad_loss=u.astype(np.float64))
+    tol = TOL[dtype]
+    per = loss.cpu().numpy().astype(np.float64)
+    e_loss = float(np.max(np.abs(per - ref["loss"]) / np.abs(ref["loss"])))
+    e_gx = norm_err(gx.float().cpu().numpy().astype(np.float64), ref["grad_x"])
+    e_gw = norm_err(gw.float().cpu().numpy().astype(np.float64), ref["grad_weight"])
+    print(f"none {name}-{dtype}: per-token loss {e_loss:.3e} gx {e_gx:.3e} gw {e_gw:.3e}")
+    assert per.shape == (T,)
+    assert e_loss <= tol["loss"] and e_gx <= tol["grad"] and e_gw <= tol["grad"]
+
+
+@pytest.mark.parametrize("pair", [0, 7])
+def test_parity_single_sm_and_sm_pair_tiles(pair):
+    """Every bf16 role on single-SM tiles (0) and on SM pairs (7), several slabs, ragged shapes."""
+    B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
     B.flce_set_backward_slab_width(2048)
     try:
-        assert B.flce_get_tuning(B.FLCE_TUNE_PAIR_GRADS) == pair
+        assert B.flce_get_tuning(B.FLCE_TUNE_SM_PAIRS) == pair
         assert_full_parity(make_inputs("ragged", dtype="bf16"), "mean", grad_loss=1.25,
                            label=f"ragged-bf16 pair={pair}")
         assert_full_parity(make_inputs("tiny", T=300, H=264, V=700, dtype="bf16", seed=21), "sum",
                            label=f"300x264x700 pair={pair}")
     finally:
-        B.flce_set_tuning(B.FLCE_TUNE_PAIR_GRADS, -1)
+        B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
         B.flce_set_backward_slab_width(0)
 
 
@@ -292,3 +315,12 @@ def test_large_batch_memory_and_sampled():
     logits_bytes = 2 * T * V  # the bf16 logits an unfused head would hold: 8.405 GB
     # peak device memory of the whole fwd+bwd, inputs and gradients included
     assert peak_total < logits_bytes
+
+
+@pytest.mark.parametrize("name", ["qwen3_head_t32768", "gemma3_head_t8192"])
+def test_second_workloads_sampled(name):
+    """The Qwen3 and Gemma3 heads of the Liger-Kernel benchmarks at full size."""
+    inp = make_inputs(name)
+    T = inp.workload.T
+    rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(T + 1).integers(0, T, 14)]))
+    _sampled_checks(inp, rows, name)

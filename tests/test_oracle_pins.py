@@ -287,3 +287,69 @@ def test_statistical_band_tiny_workload():
     loss, _ = oracle.forward(inp.x, inp.weight, inp.target, "mean")
     expect = math.log(inp.workload.V) + 0.0002 * inp.workload.H
     assert abs(loss - expect) / expect < 0.01
+
+
+# ---------------------------------------------------------------- reduction 'none'
+
+def test_none_reduction_aggregates_to_sum():
+    """'none' returns the per-token losses the 'sum' reduction adds up; an all-ones upstream
+    gradient reproduces the 'sum' gradients."""
+    T, H, V = 17, 6, 23
+    x, w, y = _rand_case(T, H, V, seed=14)
+    n = oracle.flce(x, w, y, "none", grad_loss=np.ones(T))
+    s = oracle.flce(x, w, y, "sum", grad_loss=1.0)
+    assert n["loss"].shape == (T,)
+    assert abs(n["loss"].sum() - s["loss"]) < 1e-12
+    assert np.allclose(n["grad_x"], s["grad_x"], rtol=1e-14, atol=0)
+    assert np.allclose(n["grad_weight"], s["grad_weight"], rtol=1e-13, atol=1e-16)
+
+
+def test_none_reduction_against_torch():
+    """torch float64 cross_entropy(reduction='none') with a random upstream vector."""
+    torch = pytest.importorskip("torch")
+    T, H, V = 29, 11, 41
+    x, w, y = _rand_case(T, H, V, seed=15)
+    u = np.random.default_rng(16).standard_normal(T)
+    out = oracle.flce(x, w, y, "none", grad_loss=u, chunk=7)
+    xt = torch.tensor(x, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    per = torch.nn.functional.cross_entropy(xt @ wt.T, torch.tensor(y), reduction="none")
+    (per * torch.tensor(u)).sum().backward()
+    assert np.allclose(out["loss"], per.detach().numpy(), rtol=1e-13, atol=1e-13)
+    assert np.allclose(out["grad_x"], xt.grad.numpy(), rtol=1e-11, atol=1e-14)
+    assert np.allclose(out["grad_weight"], wt.grad.numpy(), rtol=1e-11, atol=1e-14)
+
+
+def test_none_reduction_finite_differences():
+    T, H, V = 4, 3, 5
+    x, w, y = _rand_case(T, H, V, seed=17)
+    u = np.array([0.5, -1.0, 2.0, 0.25])
+    out = oracle.flce(x, w, y, "none", grad_loss=u)
+    eps = 1e-6
+
+    def L(xx, ww):
+        return float(u @ oracle.forward(xx, ww, y, "none")[0])
+
+    for i in np.ndindex(x.shape):
+        xp, xm = x.copy(), x.copy()
+        xp[i] += eps
+        xm[i] -= eps
+        assert abs((L(xp, w) - L(xm, w)) / (2 * eps) - out["grad_x"][i]) < 1e-7
+    for i in np.ndindex(w.shape):
+        wp, wm = w.copy(), w.copy()
+        wp[i] += eps
+        wm[i] -= eps
+        assert abs((L(x, wp) - L(x, wm)) / (2 * eps) - out["grad_weight"][i]) < 1e-7
+
+
+def test_none_reduction_sampled_rows_and_shape_check():
+    T, H, V = 12, 4, 9
+    x, w, y = _rand_case(T, H, V, seed=18)
+    u = np.random.default_rng(19).standard_normal(T)
+    full = oracle.flce(x, w, y, "none", grad_loss=u)
+    rows = np.array([3, 0, 11])
+    s = oracle.sampled_rows(x, w, y, rows, "none", grad_loss=u)
+    assert np.allclose(s["grad_x"], full["grad_x"][rows], rtol=0, atol=1e-15)
+    assert np.allclose(s["per_token_loss"], full["loss"][rows], rtol=0, atol=1e-15)
+    with pytest.raises(ValueError):
+        oracle.backward(x, w, y, full["lse"], "none", grad_loss=np.ones(T - 1))
