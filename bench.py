@@ -336,6 +336,52 @@ def run_ours(args, wl, rank: int, world: int, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = t.item()
 
+    # ---- single-call schedule (flce_forward_backward: no logits recompute), same inputs
+    single = None
+    if wl.dtype == "bf16" and not args.no_single_call:
+        fb_ws = B.flce_forward_backward_workspace_size(T, H, V, dt_code)
+        ws_fb = torch.empty(fb_ws, dtype=torch.uint8, device=dev)
+
+        def single_step():
+            B.flce_forward_backward(x.data_ptr(), w.data_ptr(), y.data_ptr(), T, H, V, dt_code,
+                                    red, gl.data_ptr(), loss.data_ptr(), lse.data_ptr(),
+                                    gx.data_ptr(), gw.data_ptr(), ws_fb.data_ptr(), fb_ws,
+                                    status.data_ptr(), sp)
+
+        for _ in range(args.warmup):
+            single_step()
+        torch.cuda.synchronize(dev)
+        B.flce_timing_read()
+        B.flce_timing_enable(True)
+        torch.cuda.reset_peak_memory_stats(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.steps):
+            single_step()
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        B.flce_timing_enable(False)
+        sroles = B.flce_timing_read()
+        A.check_status(status)
+        sms_ = s0.elapsed_time(s1)
+        if dist is not None:
+            t = torch.tensor([sms_], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            sms_ = t.item()
+        s_ms = sms_ / args.steps
+        single = {"ms_per_step": s_ms, "value": world * T / (s_ms * 1e-3), "unit": UNIT,
+                  "chunk_tokens": B.flce_forward_backward_chunk_tokens(T, H, V, dt_code),
+                  "flops_per_step": roofline.flops(T, H, V, "model"),
+                  "tensor_tflops": roofline.flops(T, H, V, "model") / (s_ms * 1e-3) / 1e12,
+                  "roles_ms_per_step": {r: v[1] / args.steps for r, v in sroles.items() if v[0]},
+                  "peak_mem_gb": torch.cuda.max_memory_allocated(dev) / 1e9,
+                  "workspace_gb": fb_ws / 1e9}
+        del ws_fb
+
     # ---- end-to-end: host-resident inputs, H2D copies + D2H loss read inside the timed region
     e2e_steps = max(1, min(args.steps, 5))
     h_loss = torch.empty(1, dtype=torch.float32).pin_memory()
@@ -414,6 +460,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
         "workspace_gb": max(fwd_ws, bwd_ws) / 1e9,
         "logits_bf16_gb": 2 * T * V / 1e9,
         "context": context,
+        "single_call": single,
     }
     print(json.dumps(out), flush=True)
 
@@ -425,6 +472,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-single-call", action="store_true",
+                    help="skip timing the single-call (no recompute) schedule")
     ap.add_argument("--no-context", action="store_true",
                     help="skip the PyTorch eager context measurement")
     ap.add_argument("--oracle-tokens", type=int, default=64,

@@ -130,6 +130,30 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
                   const float* grad_loss, void* grad_x, void* grad_weight,
                   void* workspace, size_t workspace_bytes, int* status, void* stream);
 
+/*
+ * Forward and backward in one call, when the upstream gradient is known before the forward (the
+ * usual case for a training loss: grad_loss = 1). The Liger-Kernel approach discussed in "[example]
+ * fused_linear_cross_entropy kernel" (Helion PR #1268) computes the gradients inside the forward
+ * over token chunks; "feat(FLCE): add helion version of fused linear cross entropy"
+ * (Liger-Kernel PR #928) calls its chunk-materialised backward "works fine". Here the logits of a
+ * chunk of tokens (at most half of all tokens and at most 1 GiB of bf16) are computed once and
+ * turned into dz in place, so the call does 6 T H V FLOPs instead of the 8 T H V of
+ * flce_forward + flce_backward, at the price of the chunk buffer and an fp32 grad_weight
+ * accumulator in the workspace.
+ *   Arguments as for flce_forward and flce_backward together: grad_loss (device, [1] or [T] for
+ *   FLCE_REDUCTION_NONE) is read by the call; loss, lse, grad_x and grad_weight are written.
+ *   bf16 with T >= 512 uses the chunked schedule; otherwise the call runs flce_forward followed
+ *   by flce_backward in the same workspace (same results as calling them).
+ * Returns FLCE_OK or a negative FLCE_ERR_* code.
+ */
+size_t flce_forward_backward_workspace_size(int64_t T, int64_t H, int64_t V, int dtype);
+/* Tokens per chunk of the single-call schedule (T itself when it does not apply), 0 if invalid. */
+int64_t flce_forward_backward_chunk_tokens(int64_t T, int64_t H, int64_t V, int dtype);
+int flce_forward_backward(const void* x, const void* weight, const int64_t* target, int64_t T,
+                          int64_t H, int64_t V, int dtype, int reduction, const float* grad_loss,
+                          float* loss, float* lse, void* grad_x, void* grad_weight,
+                          void* workspace, size_t workspace_bytes, int* status, void* stream);
+
 /* Size of the device array behind flce_forward_static_scratch (64 MiB). */
 #define FLCE_STATIC_SCRATCH_BYTES (64ull << 20)
 

@@ -11,8 +11,8 @@ import torch
 
 from . import binding as B
 
-__all__ = ["FLCEFunction", "flce", "flce_forward", "flce_backward", "check_status",
-           "FlceDeviceError"]
+__all__ = ["FLCEFunction", "flce", "flce_forward", "flce_backward", "flce_forward_backward",
+           "check_status", "FlceDeviceError"]
 
 _DTYPES = {torch.bfloat16: B.FLCE_DTYPE_BF16, torch.float32: B.FLCE_DTYPE_F32}
 
@@ -90,6 +90,30 @@ def flce_backward(x, weight, target, lse, grad_loss, reduction: str = "mean",
                     dt, B.reduction_code(reduction), grad_loss.data_ptr(), grad_x.data_ptr(),
                     grad_w.data_ptr(), ws.data_ptr(), ws_bytes, status.data_ptr(), _stream(dev))
     return grad_x, grad_w, status
+
+
+def flce_forward_backward(x, weight, target, grad_loss, reduction: str = "mean",
+                          status: torch.Tensor | None = None):
+    """Forward and backward in one call on the current stream, for an upstream gradient known in
+    advance (one element, or one per token for 'none'). Returns (loss, lse, grad_x,
+    grad_weight, status)."""
+    x, weight, target, T, H, V, dt = _prep(x, weight, target)
+    dev = x.device
+    n = T if reduction == "none" else 1
+    grad_loss = grad_loss.reshape(n).to(device=dev, dtype=torch.float32).contiguous()
+    ws_bytes = B.flce_forward_backward_workspace_size(T, H, V, dt)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    loss = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    grad_x = torch.empty_like(x)
+    grad_w = torch.empty_like(weight)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.flce_forward_backward(x.data_ptr(), weight.data_ptr(), target.data_ptr(), T, H, V, dt,
+                            B.reduction_code(reduction), grad_loss.data_ptr(), loss.data_ptr(),
+                            lse.data_ptr(), grad_x.data_ptr(), grad_w.data_ptr(), ws.data_ptr(),
+                            ws_bytes, status.data_ptr(), _stream(dev))
+    return loss, lse, grad_x, grad_w, status
 
 
 class FLCEFunction(torch.autograd.Function):

@@ -18,6 +18,8 @@ __all__ = [
     "FLCE_REDUCTION_NONE",
     "flce_forward_workspace_size", "flce_backward_workspace_size", "flce_backward_slab_width",
     "flce_set_backward_slab_width", "flce_forward", "flce_backward", "flce_strerror",
+    "flce_forward_backward", "flce_forward_backward_workspace_size",
+    "flce_forward_backward_chunk_tokens",
     "flce_version", "flce_timing_enable", "flce_timing_read", "TIMING_ROLES",
     "flce_set_tuning", "flce_get_tuning", "FLCE_TUNE_RASTER_ROWS", "FLCE_TUNE_SM_PAIRS", "FLCE_ROLE_FORWARD", "FLCE_ROLE_DZ", "FLCE_ROLE_GRADS",
     "dtype_code", "reduction_code",
@@ -80,6 +82,13 @@ def lib() -> ctypes.CDLL:
     L.flce_forward.restype = ci
     L.flce_backward.argtypes = [vp, vp, vp, vp, i64, i64, i64, ci, ci, vp, vp, vp, vp, sz, vp, vp]
     L.flce_backward.restype = ci
+    L.flce_forward_backward_workspace_size.argtypes = [i64, i64, i64, ci]
+    L.flce_forward_backward_workspace_size.restype = sz
+    L.flce_forward_backward_chunk_tokens.argtypes = [i64, i64, i64, ci]
+    L.flce_forward_backward_chunk_tokens.restype = i64
+    L.flce_forward_backward.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, vp, vp, vp, vp, vp, vp,
+                                        sz, vp, vp]
+    L.flce_forward_backward.restype = ci
     L.flce_timing_enable.argtypes = [ci]
     L.flce_timing_enable.restype = ci
     L.flce_timing_read.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]
@@ -187,6 +196,25 @@ def flce_backward(x: int, weight: int, target: int, lse: int, T: int, H: int, V:
     rc = lib().flce_backward(x, weight, target, lse, T, H, V, dtype, reduction, grad_loss,
                              grad_x, grad_weight, workspace, workspace_bytes, status, stream)
     return _check(rc, "flce_backward") if check else rc
+
+
+def flce_forward_backward_workspace_size(T: int, H: int, V: int, dtype: int) -> int:
+    return int(lib().flce_forward_backward_workspace_size(T, H, V, dtype))
+
+
+def flce_forward_backward_chunk_tokens(T: int, H: int, V: int, dtype: int) -> int:
+    return int(lib().flce_forward_backward_chunk_tokens(T, H, V, dtype))
+
+
+def flce_forward_backward(x: int, weight: int, target: int, T: int, H: int, V: int, dtype: int,
+                          reduction: int, grad_loss: int, loss: int, lse: int, grad_x: int,
+                          grad_weight: int, workspace: int, workspace_bytes: int, status: int,
+                          stream: int, check: bool = True) -> int:
+    """Enqueue forward and backward in one call (upstream gradient known in advance)."""
+    rc = lib().flce_forward_backward(x, weight, target, T, H, V, dtype, reduction, grad_loss,
+                                     loss, lse, grad_x, grad_weight, workspace, workspace_bytes,
+                                     status, stream)
+    return _check(rc, "flce_forward_backward") if check else rc
 
 
 def flce_forward_static_scratch(x: int, weight: int, target: int, T: int, H: int, V: int,

@@ -127,6 +127,77 @@ struct FwdEpi {
   }
 };
 
+// ------------------------------------------------------------------------------- chunk logits
+// Single-call forward + backward over a chunk of tokens (the logits are computed once, not
+// recomputed): like FwdEpi, each (vocab tile, token) pair leaves its (max m, sum of
+// exp(z - m)) partial and the tile holding target[t] writes z[t, target[t]]; in addition the
+// tile's logits are kept, shifted by their tile maximum, as bf16 in a chunk buffer
+// zbuf[t][v] = z[t, v] - m. The shift puts the largest logits of each tile near 0, where bf16
+// is most precise, so exp(zbuf + m - lse) recovers the dominant softmax terms accurately.
+// Two passes over TMEM: the tile maximum first, then the shifted store and the exp-sum.
+struct LogitsEpi {
+  struct Args {
+    const int64_t* target;  // chunk rows
+    float* part_m;          // [n_tiles][T]
+    float* part_s;          // [n_tiles][T]
+    float* zy;              // [T]
+    __nv_bfloat16* zbuf;    // [T][ldz]
+    int ldz;
+    int T, V;
+  };
+  struct State {};
+  static __device__ __forceinline__ void init(const Args&, State&) {}
+
+  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
+                                              uint32_t taddr) {
+    const int t = mb * kBM + row;
+    const bool valid = t < a.T;
+    const int n0 = nb * kBN;
+    const long long y = valid ? static_cast<long long>(a.target[t]) : -1ll;
+    const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
+    float m = -INFINITY, zy = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int c0 = n0 + c * 32;
+      if (c0 >= a.V) break;  // uniform across the warp
+      float v[32];
+      load_chunk(taddr, c, v);
+      const int q = rel - c * 32;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (c0 + j < a.V) m = fmaxf(m, v[j]);
+        if (j == q) zy = v[j];
+      }
+    }
+    const float ml = m * kLog2e;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      const int c0 = n0 + c * 32;
+      if (c0 >= a.V) break;
+      float v[32];
+      load_chunk(taddr, c, v);
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const float e0 = ex2(fmaf(v[j], kLog2e, -ml));
+        const float e1 = ex2(fmaf(v[j + 1], kLog2e, -ml));
+        s0 += (c0 + j < a.V) ? e0 : 0.f;
+        s1 += (c0 + j + 1 < a.V) ? e1 : 0.f;
+        v[j] -= m;
+        v[j + 1] -= m;
+      }
+      if (valid)
+        store_bf16x32(a.zbuf + static_cast<size_t>(t) * a.ldz + c0, v, 32);
+    }
+    if (valid) {
+      const size_t o = static_cast<size_t>(nb) * a.T + t;
+      a.part_m[o] = m;
+      a.part_s[o] = s0 + s1;
+      if (rel >= 0) a.zy[t] = zy;
+    }
+  }
+};
+
 // ------------------------------------------------------------------------------- backward dz
 // "[example] fused_linear_cross_entropy kernel" (Helion PR #1268), backward: the logits are
 // recomputed and turned into dz = (softmax - onehot(target)) * g in registers; here the

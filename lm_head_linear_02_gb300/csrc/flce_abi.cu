@@ -257,6 +257,49 @@ inline Range rng(const void* p, size_t bytes) {
 inline bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---- single-call forward + backward (token chunks, no logits recompute)
+
+constexpr int64_t kChunkBudgetBytes = int64_t(1) << 30;  // bf16 chunk logits per chunk
+constexpr int64_t kMinFusedTokens = 512;
+
+// The chunked single-call schedule applies to bf16 with at least 512 tokens (so a chunk never
+// holds all tokens' logits); otherwise flce_forward_backward runs flce_forward + flce_backward.
+bool fused_schedule(int64_t T, int dtype) {
+  return dtype == FLCE_DTYPE_BF16 && T >= kMinFusedTokens;
+}
+
+int64_t fused_chunk_rows(int64_t T, int64_t V) {
+  const int64_t ldz = round_up(V, kTileN);
+  int64_t c = kChunkBudgetBytes / (2 * ldz) / 256 * 256;
+  const int64_t half = round_up(cdiv(T, 2), 256);
+  if (c > half) c = half;
+  return c < 256 ? 256 : c;
+}
+
+struct FusedWs {
+  int64_t rows, ldz, n_chunks;
+  __nv_bfloat16* zbuf;
+  float *part_m, *part_s, *zy, *block_sums, *gw_acc;
+  int* counter;
+};
+
+size_t carve_fused(Carver& c, int64_t T, int64_t H, int64_t V, FusedWs* w) {
+  FusedWs r{};
+  r.rows = fused_chunk_rows(T, V);
+  r.ldz = round_up(V, kTileN);
+  r.n_chunks = cdiv(T, r.rows);
+  const int64_t nt = r.ldz / kTileN;
+  r.zbuf = static_cast<__nv_bfloat16*>(c.take(size_t(2) * r.rows * r.ldz));
+  r.part_m = static_cast<float*>(c.take(sizeof(float) * nt * r.rows));
+  r.part_s = static_cast<float*>(c.take(sizeof(float) * nt * r.rows));
+  r.zy = static_cast<float*>(c.take(sizeof(float) * r.rows));
+  r.block_sums = static_cast<float*>(c.take(sizeof(float) * cdiv(T, 256)));
+  if (r.n_chunks > 1) r.gw_acc = static_cast<float*>(c.take(sizeof(float) * V * H));
+  r.counter = static_cast<int*>(c.take(sizeof(int)));
+  if (w) *w = r;
+  return c.off;
+}
+
 int check_device(flce::Device* dev) {
   if (!flce::current_device(dev)) return FLCE_ERR_CUDA;
   if (dev->cc_major != 10 || dev->cc_minor != 3) return FLCE_ERR_UNSUPPORTED;
@@ -292,6 +335,22 @@ size_t flce_backward_workspace_size(int64_t T, int64_t H, int64_t V, int dtype) 
   if (!dims_ok(T, H, V, dtype)) return 0;
   Carver c;
   return carve_bwd(c, T, H, V, dtype, nullptr);
+}
+
+size_t flce_forward_backward_workspace_size(int64_t T, int64_t H, int64_t V, int dtype) {
+  if (!dims_ok(T, H, V, dtype)) return 0;
+  if (!fused_schedule(T, dtype)) {
+    const size_t f = flce_forward_workspace_size(T, H, V, dtype);
+    const size_t b = flce_backward_workspace_size(T, H, V, dtype);
+    return f > b ? f : b;
+  }
+  Carver c;
+  return carve_fused(c, T, H, V, nullptr);
+}
+
+int64_t flce_forward_backward_chunk_tokens(int64_t T, int64_t H, int64_t V, int dtype) {
+  if (!dims_ok(T, H, V, dtype)) return 0;
+  return fused_schedule(T, dtype) ? fused_chunk_rows(T, V) : T;
 }
 
 int64_t flce_backward_slab_width(int64_t T, int64_t H, int64_t V, int dtype) {
@@ -597,6 +656,107 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
         e = flce::timed_launch(3, s, [&] { return flce::launch_gradx_tf32(tdzh, twth, tdzl, twtl, gx); });
     }
   }
+  return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
+}
+
+int flce_forward_backward(const void* x, const void* weight, const int64_t* target, int64_t T,
+                          int64_t H, int64_t V, int dtype, int reduction, const float* grad_loss,
+                          float* loss, float* lse, void* grad_x, void* grad_weight,
+                          void* workspace, size_t workspace_bytes, int* status, void* stream) {
+  if (!x || !weight || !target || !grad_loss || !loss || !lse || !grad_x || !grad_weight ||
+      !status)
+    return FLCE_ERR_ARG;
+  if (!dims_ok(T, H, V, dtype)) return FLCE_ERR_ARG;
+  if (reduction != FLCE_REDUCTION_SUM && reduction != FLCE_REDUCTION_MEAN &&
+      reduction != FLCE_REDUCTION_NONE)
+    return FLCE_ERR_ARG;
+  const int eb = elem_bytes(dtype);
+  if ((H * eb) % 16 != 0 || !aligned16(x) || !aligned16(weight) || !aligned16(grad_x) ||
+      !aligned16(grad_weight))
+    return FLCE_ERR_UNSUPPORTED;
+  const size_t need = flce_forward_backward_workspace_size(T, H, V, dtype);
+  if (!workspace || workspace_bytes < need) return FLCE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % kAlign != 0) return FLCE_ERR_UNSUPPORTED;
+  const size_t per = reduction == FLCE_REDUCTION_NONE ? size_t(T) * 4 : 4;
+  const Range in[4] = {rng(x, size_t(T) * H * eb), rng(weight, size_t(V) * H * eb),
+                       rng(target, size_t(T) * 8), rng(grad_loss, per)};
+  const Range out[6] = {rng(loss, per), rng(lse, size_t(T) * 4),
+                        rng(grad_x, size_t(T) * H * eb), rng(grad_weight, size_t(V) * H * eb),
+                        rng(workspace, need), rng(status, sizeof(int))};
+  for (int i = 0; i < 6; ++i) {
+    for (int j = 0; j < 4; ++j)
+      if (overlap(out[i], in[j])) return FLCE_ERR_ALIAS;
+    for (int j = i + 1; j < 6; ++j)
+      if (overlap(out[i], out[j])) return FLCE_ERR_ALIAS;
+  }
+  if (!fused_schedule(T, dtype)) {
+    int rc = flce_forward(x, weight, target, T, H, V, dtype, reduction, loss, lse, workspace,
+                          workspace_bytes, status, stream);
+    if (rc != FLCE_OK) return rc;
+    return flce_backward(x, weight, target, lse, T, H, V, dtype, reduction, grad_loss, grad_x,
+                         grad_weight, workspace, workspace_bytes, status, stream);
+  }
+
+  flce::Device dev;
+  int rc = check_device(&dev);
+  if (rc != FLCE_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Carver c;
+  c.base = static_cast<uint8_t*>(workspace);
+  FusedWs w;
+  carve_fused(c, T, H, V, &w);
+  const auto DT = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const bool none = reduction == FLCE_REDUCTION_NONE;
+  CUtensorMap tw_k, tw_mn;
+  if (!flce::make_tmap_2d(&tw_k, DT, weight, H, V, H * 2, 64, kTileN) ||
+      !flce::make_tmap_2d(&tw_mn, DT, weight, H, V, H * 2, 64, 64))
+    return FLCE_ERR_CUDA;
+
+  cudaError_t e = cudaSuccess;
+  for (int64_t ci = 0; ci < w.n_chunks && e == cudaSuccess; ++ci) {
+    const int64_t t0 = ci * w.rows;
+    const int64_t rows = (T - t0) < w.rows ? (T - t0) : w.rows;
+    const uint8_t* xc = static_cast<const uint8_t*>(x) + size_t(t0) * H * 2;
+    CUtensorMap tx_k, tx_mn, tz_k, tz_mn;
+    if (!flce::make_tmap_2d(&tx_k, DT, xc, H, rows, H * 2, 64, kTileM) ||
+        !flce::make_tmap_2d(&tx_mn, DT, xc, H, rows, H * 2, 64, 64) ||
+        !flce::make_tmap_2d(&tz_k, DT, w.zbuf, V, rows, w.ldz * 2, 64, kTileM) ||
+        !flce::make_tmap_2d(&tz_mn, DT, w.zbuf, V, rows, w.ldz * 2, 64, 64))
+      return FLCE_ERR_CUDA;
+    flce::ChunkLaunch cl{};
+    cl.target = target + t0;
+    cl.lse = lse + t0;
+    cl.row_scale = none ? grad_loss + t0 : nullptr;
+    cl.grad_loss = none ? nullptr : grad_loss;
+    cl.scale = reduction == FLCE_REDUCTION_MEAN ? 1.0f / float(T) : 1.0f;
+    cl.zbuf = w.zbuf;
+    cl.ldz = int(w.ldz);
+    cl.part_m = w.part_m;
+    cl.part_s = w.part_s;
+    cl.zy = w.zy;
+    cl.grad_x_rows = static_cast<uint8_t*>(grad_x) + size_t(t0) * H * 2;
+    cl.grad_w = grad_weight;
+    cl.gw_acc = w.gw_acc;
+    cl.gw_mode = w.n_chunks == 1 ? 0 : (ci == 0 ? 1 : (ci == w.n_chunks - 1 ? 3 : 2));
+    cl.tile_counter = w.counter;
+    cl.rows = int(rows);
+    cl.H = int(H);
+    cl.V = int(V);
+    cl.status = status;
+    cl.sms = dev.sms;
+    cl.stream = s;
+    e = flce::timed_launch(0, s, [&] { return flce::launch_chunk_logits(tx_k, tw_k, cl); });
+    if (e == cudaSuccess)
+      e = flce::launch_combine_rows(w.part_m, w.part_s, w.zy, target + t0, int(rows), int(V),
+                                    int(w.ldz / kTileN), lse + t0, w.block_sums + t0 / 256,
+                                    none ? loss + t0 : nullptr, status, s);
+    if (e == cudaSuccess) e = flce::launch_form_dz(cl);
+    if (e == cudaSuccess)
+      e = flce::timed_launch(4, s,
+                             [&] { return flce::launch_chunk_grads(tz_k, tw_mn, tz_mn, tx_mn, cl); });
+  }
+  if (e == cudaSuccess && !none)
+    e = flce::launch_finalize(w.block_sums, int(cdiv(T, 256)), int(T), reduction, loss, s);
   return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
 }
 

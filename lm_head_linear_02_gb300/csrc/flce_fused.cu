@@ -1,0 +1,95 @@
+// flce_fused.cu - forward and backward in one call, over chunks of tokens, without recomputing
+// the logits (the "compute the gradients during the forward" schedule of the Liger-Kernel
+// discussion in "[example] fused_linear_cross_entropy kernel", Helion PR #1268, and of
+// "feat(FLCE): add helion version of fused linear cross entropy", Liger-Kernel PR #928: "chunk
+// backward (recompute chunk logits then accumulate dx and dw)"; here nothing is recomputed).
+//
+// Per chunk of Tc tokens (never all T: the chunk buffer holds at most half the tokens' logits):
+//   1. logits  : z = x_c . W^T (tcgen05), kept as bf16 z - m_tile plus lse partials (LogitsEpi)
+//   2. combine : lse, per-token loss / loss block sums of the chunk rows (k_fwd_combine)
+//   3. form dz : dz = (exp(z - lse) - onehot) * row scale, in place, bf16 (k_form_dz)
+//   4. grads   : grad_x[chunk] = dz . W (complete, K = V) and grad_W (+)= dz^T . x_c (K = Tc,
+//                fp32 accumulation over chunks in chunk order), one launch, dynamic tiles
+// FLOPs: 6 T H V (forward + two gradient contractions) instead of 8 T H V with recompute.
+#include "epilogues.cuh"
+#include "flce_internal.h"
+
+namespace flce {
+
+// dz[t][v] = (exp(zbuf[t][v] + m[v / 256][t] - lse[t]) - [v == target[t]]) * row_scale[t] for
+// v < V, 0 for V <= v < ldz; 8 consecutive columns (16 bytes) per thread, in place.
+__global__ void __launch_bounds__(256)
+    k_form_dz(__nv_bfloat16* __restrict__ zbuf, int ldz, int rows, int V,
+              const float* __restrict__ part_m, const float* __restrict__ lse,
+              const int64_t* __restrict__ target, const float* __restrict__ row_scale) {
+  const int vecs = ldz / 8;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(rows) * vecs) return;
+  const int t = static_cast<int>(idx / vecs);
+  const int v0 = static_cast<int>(idx - static_cast<int64_t>(t) * vecs) * 8;
+  uint4* p = reinterpret_cast<uint4*>(zbuf + static_cast<size_t>(t) * ldz + v0);
+  const float off = (part_m[static_cast<size_t>(v0 / kBN) * rows + t] - lse[t]) * kLog2e;
+  const long long y = static_cast<long long>(target[t]);
+  const float rs = row_scale ? row_scale[t] : 1.0f;
+  uint4 w = *p;
+  uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+  float d[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lo = __uint_as_float(u[j] << 16);
+    const float hi = __uint_as_float(u[j] & 0xffff0000u);
+    d[2 * j] = lo;
+    d[2 * j + 1] = hi;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int v = v0 + j;
+    float e = ex2(fmaf(d[j], kLog2e, off));
+    if (v == y) e -= 1.0f;
+    d[j] = v < V ? e * rs : 0.0f;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) u[j] = pack_bf16x2(d[2 * j], d[2 * j + 1]);
+  *p = w;
+}
+
+cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
+                                const ChunkLaunch& c) {
+  LogitsEpi::Args ea{c.target, c.part_m, c.part_s, c.zy, c.zbuf, c.ldz, c.rows, c.V};
+  GemmGrid g{};
+  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, kBM, 0);
+  g.num_problems = 1;
+  g.status = c.status;
+  return launch_gemm<false, LogitsEpi, NoEpi>(tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{}, c.sms,
+                                              c.stream);
+}
+
+cudaError_t launch_form_dz(const ChunkLaunch& c) {
+  const int64_t n = static_cast<int64_t>(c.rows) * (c.ldz / 8);
+  const int64_t blocks = (n + 255) / 256;
+  k_form_dz<<<static_cast<unsigned>(blocks), 256, 0, c.stream>>>(
+      c.zbuf, c.ldz, c.rows, c.V, c.part_m, c.lse, c.target, c.row_scale);
+  return cudaGetLastError();
+}
+
+// grad_x rows of the chunk (A = dz K-major, B = W MN-major, K = V: few long tiles, listed
+// first) and grad_W (A = dz MN-major, B = x_c MN-major, K = Tc: many short tiles) in one launch
+// whose CTAs take tiles from a shared counter, longest first, so the long tiles spread evenly.
+cudaError_t launch_chunk_grads(const CUtensorMap& tz_k, const CUtensorMap& tw_mn,
+                               const CUtensorMap& tz_mn, const CUtensorMap& tx_mn,
+                               const ChunkLaunch& c) {
+  typename GradXEpi<false>::Args ex{nullptr, c.grad_x_rows, c.grad_loss, c.scale,
+                                    c.rows,  c.H,           0};
+  typename GradXEpi<false>::Args ew{c.gw_acc, c.grad_w, c.grad_loss, c.scale,
+                                    c.V,      c.H,      c.gw_mode};
+  GemmGrid g{};
+  g.p[0] = make_problem(c.rows, c.H, c.V, 64, false, true, kBM, 0);
+  g.p[1] = make_problem(c.V, c.H, c.rows, 64, true, true, kBM, g.p[0].m_tiles * g.p[0].n_tiles);
+  g.num_problems = 2;
+  g.status = c.status;
+  g.tile_counter = c.tile_counter;
+  return launch_gemm<false, GradXEpi<false>, GradXEpi<false>>(tz_k, tw_mn, tz_mn, tx_mn, g, ex, ew,
+                                                              c.sms, c.stream);
+}
+
+}  // namespace flce

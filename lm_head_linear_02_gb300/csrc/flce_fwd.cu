@@ -95,16 +95,29 @@ static cudaError_t launch_forward(const CUtensorMap& tx, const CUtensorMap& tw,
 
 // The combine (lse, per-token loss, block sums) and finalize kernels after the projection.
 static cudaError_t launch_combine(const FwdLaunch& p) {
-  cudaError_t e;
   const int n_tiles = (p.V + kBN - 1) / kBN;
-  const int nblk = (p.T + kCombineThreads - 1) / kCombineThreads;
   const bool none = p.reduction == FLCE_REDUCTION_NONE;
-  k_fwd_combine<<<nblk, kCombineThreads, 0, p.stream>>>(p.part_m, p.part_s, p.zy, p.target, p.T,
-                                                        p.V, n_tiles, p.lse, p.block_sums,
-                                                        none ? p.loss : nullptr, p.status);
-  e = cudaGetLastError();
+  cudaError_t e = launch_combine_rows(p.part_m, p.part_s, p.zy, p.target, p.T, p.V, n_tiles,
+                                      p.lse, p.block_sums, none ? p.loss : nullptr, p.status,
+                                      p.stream);
   if (e != cudaSuccess || none) return e;
-  k_fwd_finalize<<<1, 256, 0, p.stream>>>(p.block_sums, nblk, p.T, p.reduction, p.loss);
+  return launch_finalize(p.block_sums, (p.T + kCombineThreads - 1) / kCombineThreads, p.T,
+                         p.reduction, p.loss, p.stream);
+}
+
+cudaError_t launch_combine_rows(const float* part_m, const float* part_s, const float* zy,
+                                const int64_t* target, int rows, int V, int n_tiles, float* lse,
+                                float* block_sums, float* per_token, int* status,
+                                cudaStream_t stream) {
+  const int nblk = (rows + kCombineThreads - 1) / kCombineThreads;
+  k_fwd_combine<<<nblk, kCombineThreads, 0, stream>>>(part_m, part_s, zy, target, rows, V, n_tiles,
+                                                      lse, block_sums, per_token, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* block_sums, int n_blocks, int T, int reduction,
+                            float* loss, cudaStream_t stream) {
+  k_fwd_finalize<<<1, 256, 0, stream>>>(block_sums, n_blocks, T, reduction, loss);
   return cudaGetLastError();
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
@@ -64,6 +65,16 @@ cudaError_t launch_forward_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_
                                 const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
                                 const FwdLaunch& p);
 
+// Merge the per-vocab-tile partials of `rows` tokens (all pointers already offset to those rows)
+// into lse, one loss sum per 256 rows (block_sums) and, if per_token is non-null, l[t].
+cudaError_t launch_combine_rows(const float* part_m, const float* part_s, const float* zy,
+                                const int64_t* target, int rows, int V, int n_tiles, float* lse,
+                                float* block_sums, float* per_token, int* status,
+                                cudaStream_t stream);
+// loss[0] = sum of n_blocks block sums (fp64, fixed order), / T for the mean reduction.
+cudaError_t launch_finalize(const float* block_sums, int n_blocks, int T, int reduction,
+                            float* loss, cudaStream_t stream);
+
 // ---------------------------------------------------------------- backward launchers (flce_bwd.cu)
 struct DzLaunch {
   const int64_t* target;
@@ -118,6 +129,35 @@ cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
 cudaError_t launch_gradx_tf32(const CUtensorMap& tdz_hi, const CUtensorMap& twt_hi,
                               const CUtensorMap& tdz_lo, const CUtensorMap& twt_lo,
                               const GradXLaunch& p);
+
+// ---------------------------------------------------------------- single-call fwd+bwd (flce_fused.cu)
+struct ChunkLaunch {
+  const int64_t* target;   // chunk rows
+  float* lse;              // chunk rows
+  const float* row_scale;  // per-token upstream gradient of the chunk rows ('none') or null
+  const float* grad_loss;  // global upstream gradient (sum/mean) or null ('none')
+  float scale;             // 1 or 1/T
+  __nv_bfloat16* zbuf;     // [rows][ldz] chunk logits (shifted) / dz
+  int ldz;
+  float *part_m, *part_s, *zy;  // [ldz / 256][rows], [ldz / 256][rows], [rows]
+  void* grad_x_rows;       // grad_x + t0 * H
+  void* grad_w;
+  float* gw_acc;           // fp32 [V][H] accumulator across chunks
+  int gw_mode;             // 0 only chunk, 1 first, 2 middle, 3 last
+  int* tile_counter;
+  int rows, H, V;
+  int* status;
+  int sms;
+  cudaStream_t stream;
+};
+// logits of the chunk: x_c K-major {64 x 128}, W K-major {64 x 256}
+cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
+                                const ChunkLaunch& c);
+cudaError_t launch_form_dz(const ChunkLaunch& c);
+// grads: dz K-major {64 x 128} and W MN-major {64 x 64}; dz MN-major and x_c MN-major {64 x 64}
+cudaError_t launch_chunk_grads(const CUtensorMap& tz_k, const CUtensorMap& tw_mn,
+                               const CUtensorMap& tz_mn, const CUtensorMap& tx_mn,
+                               const ChunkLaunch& c);
 
 // fp32 -> (hi, lo) TF32 split, optionally transposed: src [rows][cols] -> hi/lo [rows][ld_out]
 // or, with transpose, hi/lo [cols][ld_out] (ld_out >= rows).

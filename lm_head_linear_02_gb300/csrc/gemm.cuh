@@ -43,8 +43,14 @@ struct GemmGrid {
   GemmProblem p[2];
   int num_problems;
   int num_tiles;
-  int* status;  // device status word (FLCE_STATUS_* bits)
+  int* status;        // device status word (FLCE_STATUS_* bits)
+  int* tile_counter;  // null: CTA b takes tiles b, b + grid, ...; else a zeroed device int that
+                      // hands out tiles in list order to whichever CTA is free (dynamic)
 };
+
+// Depth of the per-CTA queue through which the producer hands tile indices to the MMA thread
+// and the epilogue warps.
+constexpr int kTileQueue = 4;
 
 // The fields of the problem a tile belongs to, selected field by field (no dynamic indexing of
 // the parameter array, so everything stays in registers).
@@ -108,13 +114,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + G::kRingBytes);
-  // bars[0..S) full, [S..2S) empty, [2S..2S+2) tmem_full, [2S+2..2S+4) tmem_empty, [2S+4] drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::kStages + 5);
+  // bars[0..S) full, [S..2S) empty, [2S..2S+2) tmem_full, [2S+2..2S+4) tmem_empty, [2S+4] drain,
+  // [2S+5..2S+5+Q) tile-queue full, [2S+5+Q..2S+5+2Q) tile-queue empty
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * G::kStages + 5 + 2 * kTileQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   // Pipeline counters kept in shared memory so that an aborted CTA can wait out its own
   // copies and MMAs still in flight before it frees TMEM and exits.
   int* issued_fills = reinterpret_cast<int*>(tmem_slot + 2);
   int* consumed_fills = reinterpret_cast<int*>(tmem_slot + 3);
+  volatile int* tile_q = reinterpret_cast<volatile int*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -125,6 +133,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * G::kStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * G::kStages + 2 + a); };
   auto drain_bar = [&]() { return bar0 + 8u * (2 * G::kStages + 4); };
+  auto tq_full = [&](int q) { return bar0 + 8u * (2 * G::kStages + 5 + q); };
+  auto tq_empty = [&](int q) { return bar0 + 8u * (2 * G::kStages + 5 + kTileQueue + q); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::kStages; ++s) {
@@ -136,6 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), 128);
     }
     mbar_init(drain_bar(), 1);
+    for (int q = 0; q < kTileQueue; ++q) {
+      mbar_init(tq_full(q), 1);   // the producer publishes a tile index
+      mbar_init(tq_empty(q), 5);  // the MMA thread and the 4 epilogue warps have read it
+    }
     *abort_flag = 0;
     *issued_fills = 0;
     *consumed_fills = 0;
@@ -165,7 +179,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int fills = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+      int qslot = 0;
+      uint32_t qphase = 0;
+      for (int i = 0; ok; ++i) {
+        // Next tile (static stride or the shared counter); -1 ends the queue for the consumers.
+        int t = g.tile_counter ? atomicAdd(g.tile_counter, 1)
+                               : static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+        if (t >= g.num_tiles) t = -1;
+        if (!mbar_wait(tq_empty(qslot), qphase ^ 1u, g.status, abort_flag)) break;
+        tile_q[qslot] = t;
+        mbar_arrive(tq_full(qslot));
+        if (++qslot == kTileQueue) {
+          qslot = 0;
+          qphase ^= 1u;
+        }
+        if (t < 0) break;
         const TileInfo ti = map_tile(g, t);
         const CUtensorMap* ta = (!kTF32x3 && ti.prob) ? &tA1 : &tA0;
         const CUtensorMap* tb = (!kTF32x3 && ti.prob) ? &tB1 : &tB0;
@@ -216,7 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       int consumed = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < g.num_tiles && ok; t += gridDim.x) {
+      int qslot = 0;
+      uint32_t qphase = 0;
+      while (ok) {
+        if (!mbar_wait(tq_full(qslot), qphase, g.status, abort_flag)) break;
+        const int t = tile_q[qslot];
+        mbar_arrive(tq_empty(qslot));
+        if (++qslot == kTileQueue) {
+          qslot = 0;
+          qphase ^= 1u;
+        }
+        if (t < 0) break;
         const TileInfo ti = map_tile(g, t);
         const bool a_mn = !kTF32x3 && ti.a_mn != 0;
         const bool b_mn = !kTF32x3 && ti.b_mn != 0;
@@ -283,7 +321,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     typename Epi1::State st1;
     Epi0::init(e0, st0);
     Epi1::init(e1, st1);
-    for (int t = blockIdx.x; t < g.num_tiles; t += gridDim.x) {
+    int qslot = 0;
+    uint32_t qphase = 0;
+    while (true) {
+      if (!mbar_wait(tq_full(qslot), qphase, g.status, abort_flag)) break;
+      const int t = tile_q[qslot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tq_empty(qslot));
+      if (++qslot == kTileQueue) {
+        qslot = 0;
+        qphase ^= 1u;
+      }
+      if (t < 0) break;
       if (!mbar_wait(tfull_bar(acc), acc_phase, g.status, abort_flag)) break;
       tc_fence_after_sync();
       __syncwarp();
@@ -362,6 +411,10 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUte
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
   if (e != cudaSuccess) return e;
   finish_grid(g);
+  if (g.tile_counter) {
+    e = cudaMemsetAsync(g.tile_counter, 0, sizeof(int), stream);
+    if (e != cudaSuccess) return e;
+  }
   const int grid = g.num_tiles < sms ? g.num_tiles : sms;
   kern<<<grid, kThreads, G::kSmemBytes, stream>>>(a0, b0, a1, b1, g, e0, e1);
   return cudaGetLastError();

@@ -224,16 +224,20 @@ def test_autograd_function():
 
 # ------------------------------------------------------------------ Llama-3 head, full sizes
 
-def _sampled_checks(inp, rows, label):
-    """Full-size run: sampled rows vs the oracle, plus size-independent properties."""
+def _sampled_checks(inp, rows, label, fused=False):
+    """Full-size run: sampled rows vs the oracle, plus size-independent properties.
+    fused: one flce_forward_backward call instead of flce_forward + flce_backward."""
     T, H, V = inp.workload.T, inp.workload.H, inp.workload.V
     x, w, y = to_device(inp)
     torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats()
     base = torch.cuda.memory_allocated()
-    loss_t, lse_t, status = A.flce_forward(x, w, y, "mean")
     g = torch.ones(1, dtype=torch.float32, device="cuda")
-    gx_t, gw_t, status = A.flce_backward(x, w, y, lse_t, g, "mean", status=status)
+    if fused:
+        loss_t, lse_t, gx_t, gw_t, status = A.flce_forward_backward(x, w, y, g, "mean")
+    else:
+        loss_t, lse_t, status = A.flce_forward(x, w, y, "mean")
+        gx_t, gw_t, status = A.flce_backward(x, w, y, lse_t, g, "mean", status=status)
     torch.cuda.synchronize()
     A.check_status(status)
     peak_total = torch.cuda.max_memory_allocated()
@@ -324,3 +328,79 @@ def test_second_workloads_sampled(name):
     T = inp.workload.T
     rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(T + 1).integers(0, T, 14)]))
     _sampled_checks(inp, rows, name)
+
+
+# ------------------------------------------------------------------ single-call forward + backward
+
+def run_fused(x, w, y, reduction, grad_loss):
+    T = x.shape[0]
+    g = (torch.from_numpy(np.asarray(grad_loss, dtype=np.float32)).cuda()
+         if reduction == "none" else torch.full((1,), float(grad_loss), device="cuda"))
+    loss, lse, gx, gw, status = A.flce_forward_backward(x, w, y, g, reduction)
+    torch.cuda.synchronize()
+    A.check_status(status)
+    lv = loss.cpu().numpy().astype(np.float64)
+    return (lv if reduction == "none" else float(lv[0]), lse.cpu().numpy().astype(np.float64),
+            gx.float().cpu().numpy().astype(np.float64), gw.float().cpu().numpy().astype(np.float64))
+
+
+@pytest.mark.parametrize("name,T,H,V,dtype,reduction", [
+    ("ragged", None, None, None, "bf16", "mean"),   # 2 chunks of 768 tokens, ragged everywhere
+    ("ragged", None, None, None, "bf16", "sum"),
+    ("ragged", None, None, None, "bf16", "none"),
+    ("llama2_head", None, None, None, "bf16", "mean"),  # 2 chunks of 2048
+    ("tiny", 600, 264, 513, "bf16", "mean"),        # chunk 512 + ragged 88-token chunk
+    ("tiny", 300, 200, 700, "bf16", "mean"),        # fewer than 512 tokens: two-call schedule
+    ("ragged", None, None, None, "f32", "mean"),    # fp32: two-call schedule
+])
+def test_parity_forward_backward_single_call(name, T, H, V, dtype, reduction):
+    inp = make_inputs(name, T=T, H=H, V=V, dtype=dtype, seed=None if T is None else 31 + T)
+    Tn = inp.workload.T
+    gl = (np.random.default_rng(Tn).standard_normal(Tn) if reduction == "none" else 1.5)
+    x, w, y = to_device(inp)
+    loss, lse, gx, gw = run_fused(x, w, y, reduction, gl)
+    ref = oracle.flce(inp.x, inp.weight, inp.target, reduction, grad_loss=gl)
+    tol = TOL[dtype]
+    if reduction == "none":
+        rel = float(np.max(np.abs(loss - ref["loss"]) / np.abs(ref["loss"])))
+    else:
+        rel = abs(loss - ref["loss"]) / abs(ref["loss"])
+    e_lse = float(np.abs(lse - ref["lse"]).max())
+    e_gx = norm_err(gx, ref["grad_x"])
+    e_gw = norm_err(gw, ref["grad_weight"])
+    chunk = B.flce_forward_backward_chunk_tokens(Tn, inp.workload.H, inp.workload.V,
+                                                 B.dtype_code(dtype))
+    print(f"single call {name} T={Tn} chunk={chunk} {dtype}/{reduction}: loss {rel:.3e} "
+          f"lse {e_lse:.3e} gx {e_gx:.3e} gw {e_gw:.3e}")
+    assert rel <= tol["loss"] and e_lse <= tol["lse"]
+    assert e_gx <= tol["grad"] and e_gw <= tol["grad"]
+
+
+def test_single_call_is_deterministic_and_agrees_with_two_calls():
+    """Dynamic tile scheduling must not change a bit; the two schedules agree within tolerance."""
+    inp = make_inputs("llama2_head")
+    x, w, y = to_device(inp)
+    a = run_fused(x, w, y, "mean", 1.0)
+    b = run_fused(x, w, y, "mean", 1.0)
+    assert a[0] == b[0]
+    for u, v in zip(a[1:], b[1:]):
+        assert np.array_equal(u, v)
+    c = run_gpu(x, w, y, "mean")
+    assert abs(a[0] - c[0]) / abs(c[0]) < 1e-5
+    assert np.abs(a[1] - c[1]).max() < 1e-3
+    assert norm_err(a[2], c[2]) < 2e-2 and norm_err(a[3], c[3]) < 2e-2
+
+
+def test_single_call_full_size_headline():
+    inp = make_inputs("llama3_head_t16384")
+    T = inp.workload.T
+    rows = np.unique(np.concatenate([[0, 4095, 4096, T - 1], np.random.default_rng(3).integers(0, T, 12)]))
+    _sampled_checks(inp, rows, "single call llama3_head_t16384", fused=True)
+
+
+def test_single_call_large_batch_memory():
+    inp = make_inputs("llama3_head_t32768")
+    T, V = inp.workload.T, inp.workload.V
+    rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(9).integers(0, T, 8)]))
+    peak_total = _sampled_checks(inp, rows, "single call llama3_head_t32768", fused=True)
+    assert peak_total < 2 * T * V  # below the bf16 logits of all tokens (8.4 GB)
