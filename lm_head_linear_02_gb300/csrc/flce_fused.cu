@@ -13,6 +13,7 @@
 // FLOPs: 6 T H V (forward + two gradient contractions) instead of 8 T H V with recompute.
 #include "epilogues.cuh"
 #include "flce_internal.h"
+#include "gemm_pair.cuh"
 
 namespace flce {
 
@@ -74,7 +75,8 @@ cudaError_t launch_form_dz(const ChunkLaunch& c) {
 
 // grad_x rows of the chunk (A = dz K-major, B = W MN-major, K = V: few long tiles, listed
 // first) and grad_W (A = dz MN-major, B = x_c MN-major, K = Tc: many short tiles) in one launch
-// whose CTAs take tiles from a shared counter, longest first, so the long tiles spread evenly.
+// whose CTAs (or CTA pairs) take tiles from a shared counter, longest first, so the long tiles
+// spread evenly.
 cudaError_t launch_chunk_grads(const CUtensorMap& tz_k, const CUtensorMap& tw_mn,
                                const CUtensorMap& tz_mn, const CUtensorMap& tx_mn,
                                const ChunkLaunch& c) {
@@ -82,12 +84,18 @@ cudaError_t launch_chunk_grads(const CUtensorMap& tz_k, const CUtensorMap& tw_mn
                                     c.rows,  c.H,           0};
   typename GradXEpi<false>::Args ew{c.gw_acc, c.grad_w, c.grad_loss, c.scale,
                                     c.V,      c.H,      c.gw_mode};
+  const bool pairs = (pair_roles(c.sms) & FLCE_ROLE_GRADS) != 0;
+  const int tile_rows = pairs ? 256 : kBM;
   GemmGrid g{};
-  g.p[0] = make_problem(c.rows, c.H, c.V, 64, false, true, kBM, 0);
-  g.p[1] = make_problem(c.V, c.H, c.rows, 64, true, true, kBM, g.p[0].m_tiles * g.p[0].n_tiles);
+  g.p[0] = make_problem(c.rows, c.H, c.V, 64, false, true, tile_rows, 0);
+  g.p[1] = make_problem(c.V, c.H, c.rows, 64, true, true, tile_rows,
+                        g.p[0].m_tiles * g.p[0].n_tiles);
   g.num_problems = 2;
   g.status = c.status;
   g.tile_counter = c.tile_counter;
+  if (pairs)
+    return launch_pair<GradXEpi<false>, GradXEpi<false>>(tz_k, tw_mn, tz_mn, tx_mn, g, ex, ew, c.sms,
+                                                         c.stream);
   return launch_gemm<false, GradXEpi<false>, GradXEpi<false>>(tz_k, tw_mn, tz_mn, tx_mn, g, ex, ew,
                                                               c.sms, c.stream);
 }

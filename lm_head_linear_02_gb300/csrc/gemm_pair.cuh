@@ -45,11 +45,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairRingBytes);
   // bars: [0,S) full, [S,2S) empty, [2S,2S+2) tmem_full, [2S+2,2S+4) tmem_empty, [2S+4] drain
-  uint32_t* slots = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5);
+  // [2S+5, 2S+5+Q) tile-queue full, [2S+5+Q, 2S+5+2Q) tile-queue empty (used in the leader)
+  uint32_t* slots = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5 + 2 * kTileQueue);
   uint32_t* tmem_slot = slots;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
   int* issued_fills = reinterpret_cast<int*>(slots + 2);
   int* consumed_fills = reinterpret_cast<int*>(slots + 3);
+  volatile int* tile_q = reinterpret_cast<volatile int*>(slots + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -62,6 +64,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kPairStages + 2 + a); };
   auto drain_bar = [&]() { return bar0 + 8u * (2 * kPairStages + 4); };
+  auto tq_full = [&](int q) { return bar0 + 8u * (2 * kPairStages + 5 + q); };
+  auto tq_empty = [&](int q) { return bar0 + 8u * (2 * kPairStages + 5 + kTileQueue + q); };
+  // Tile indices flow through a small queue in each CTA: the leader's producer takes the next
+  // tile (fixed stride or the shared counter) and writes it into both CTAs' queues; the
+  // leader's MMA thread, the peer's producer and the epilogue warps of both CTAs read it and
+  // release the slot back to the leader (1 + 1 + 4 + 4 = 10 arrivals).
+  auto tq_release = [&](int q) {
+    if (leader)
+      mbar_arrive(tq_empty(q));
+    else
+      mbar_arrive_cluster(mapa_shared(tq_empty(q), 0));
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
@@ -73,6 +87,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), 8);  // leader: 4 epilogue warps x 2 CTAs
     }
     mbar_init(drain_bar(), 1);
+    for (int q = 0; q < kTileQueue; ++q) {
+      mbar_init(tq_full(q), 1);
+      mbar_init(tq_empty(q), 10);
+    }
     *abort_flag = 0;
     *issued_fills = 0;
     *consumed_fills = 0;
@@ -105,7 +123,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int fills = 0;
       bool ok = true;
-      for (int t = cluster_id; t < g.num_tiles && ok; t += n_clusters) {
+      int qslot = 0;
+      uint32_t qphase = 0;
+      for (int i = 0; ok; ++i) {
+        int t;
+        if (leader) {
+          t = g.tile_counter ? atomicAdd(g.tile_counter, 1) : cluster_id + i * n_clusters;
+          if (t >= g.num_tiles) t = -1;
+          if (!mbar_wait_cluster(tq_empty(qslot), qphase ^ 1u, g.status, abort_flag)) break;
+          tile_q[qslot] = t;
+          st_shared_cluster(mapa_shared(smem_u32(const_cast<int*>(tile_q + qslot)), 1), t);
+          mbar_arrive(tq_full(qslot));
+          mbar_arrive_cluster(mapa_shared(tq_full(qslot), 1));
+        } else {
+          if (!mbar_wait_cluster(tq_full(qslot), qphase, g.status, abort_flag)) break;
+          t = tile_q[qslot];
+          tq_release(qslot);
+        }
+        if (++qslot == kTileQueue) {
+          qslot = 0;
+          qphase ^= 1u;
+        }
+        if (t < 0) break;
         const TileInfo pt = map_tile(g, t);
         const CUtensorMap* ta = pt.prob ? &tA1 : &tA0;
         const CUtensorMap* tb = pt.prob ? &tB1 : &tB0;
@@ -154,7 +193,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t acc_phase = 0;
       int consumed = 0;
       bool ok = true;
-      for (int t = cluster_id; t < g.num_tiles && ok; t += n_clusters) {
+      int qslot = 0;
+      uint32_t qphase = 0;
+      while (ok) {
+        if (!mbar_wait(tq_full(qslot), qphase, g.status, abort_flag)) break;
+        const int t = tile_q[qslot];
+        tq_release(qslot);
+        if (++qslot == kTileQueue) {
+          qslot = 0;
+          qphase ^= 1u;
+        }
+        if (t < 0) break;
         const TileInfo pt = map_tile(g, t);
         const bool a_mn = pt.a_mn != 0, b_mn = pt.b_mn != 0;
         const int k_blocks = pt.k_blocks;
@@ -209,7 +258,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     typename Epi1::State st1;
     Epi0::init(e0, st0);
     Epi1::init(e1, st1);
-    for (int t = cluster_id; t < g.num_tiles; t += n_clusters) {
+    int qslot = 0;
+    uint32_t qphase = 0;
+    while (true) {
+      if (!mbar_wait_cluster(tq_full(qslot), qphase, g.status, abort_flag)) break;
+      const int t = tile_q[qslot];
+      __syncwarp();
+      if (lane == 0) tq_release(qslot);
+      if (++qslot == kTileQueue) {
+        qslot = 0;
+        qphase ^= 1u;
+      }
+      if (t < 0) break;
       if (!mbar_wait(tfull_bar(acc), acc_phase, g.status, abort_flag)) break;
       tc_fence_after_sync();
       __syncwarp();
@@ -298,6 +358,10 @@ cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& b0, const CUte
   if (e != cudaSuccess) return e;
   const int max_clusters = pair_resident_clusters(kern, sms);
   finish_grid(g);
+  if (g.tile_counter) {
+    e = cudaMemsetAsync(g.tile_counter, 0, sizeof(int), stream);
+    if (e != cudaSuccess) return e;
+  }
   const int clusters = g.num_tiles < max_clusters ? g.num_tiles : max_clusters;
   kern<<<2 * clusters, kThreads, kPairSmemBytes, stream>>>(a0, b0, a1, b1, g, e0, e1);
   return cudaGetLastError();

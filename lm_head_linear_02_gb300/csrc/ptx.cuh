@@ -271,6 +271,11 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
+// Store a 32-bit value into shared memory of a CTA of the cluster (cluster-window address).
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, int v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // TMA load into this CTA's shared memory whose completion is counted on an mbarrier that may
 // live in either CTA of the pair (`bar` is a cluster-window address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm,

@@ -376,6 +376,26 @@ def test_parity_forward_backward_single_call(name, T, H, V, dtype, reduction):
     assert e_gx <= tol["grad"] and e_gw <= tol["grad"]
 
 
+@pytest.mark.parametrize("pair", [0, 4])
+def test_single_call_gradient_tiles_single_sm_and_sm_pairs(pair):
+    """The single call's dynamically scheduled gradient launch on single SMs and on SM pairs."""
+    B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
+    try:
+        for name, red in [("ragged", "mean"), ("llama2_head", "none")]:
+            inp = make_inputs(name, dtype="bf16")
+            Tn = inp.workload.T
+            gl = np.random.default_rng(5).standard_normal(Tn) if red == "none" else 1.0
+            x, w, y = to_device(inp)
+            loss, lse, gx, gw = run_fused(x, w, y, red, gl)
+            ref = oracle.flce(inp.x, inp.weight, inp.target, red, grad_loss=gl)
+            e_gx = norm_err(gx, ref["grad_x"])
+            e_gw = norm_err(gw, ref["grad_weight"])
+            print(f"single call pair={pair} {name}/{red}: gx {e_gx:.3e} gw {e_gw:.3e}")
+            assert e_gx <= TOL["bf16"]["grad"] and e_gw <= TOL["bf16"]["grad"]
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
+
+
 def test_single_call_is_deterministic_and_agrees_with_two_calls():
     """Dynamic tile scheduling must not change a bit; the two schedules agree within tolerance."""
     inp = make_inputs("llama2_head")
