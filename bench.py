@@ -55,6 +55,23 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest of each rank's value (a timed region ends when the slowest rank is done).
+    Single-process runs (dist None) return the value itself."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units processed by all ranks together per second of the slowest rank."""
+    return world * units_per_rank / seconds
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -331,10 +348,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
     fwd_ms = [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(args.steps)]
     bwd_ms = [ev[2 * k + 1].elapsed_time(ev[2 * k + 2]) for k in range(args.steps)]
     peak_mem = torch.cuda.max_memory_allocated(dev)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = t.item()
+    total_ms = max_over_ranks(total_ms, dist, dev)
 
     # ---- single-call schedule (flce_forward_backward: no logits recompute), same inputs
     single = None
@@ -368,12 +382,9 @@ def run_ours(args, wl, rank: int, world: int, dist):
         sroles = B.flce_timing_read()
         A.check_status(status)
         sms_ = s0.elapsed_time(s1)
-        if dist is not None:
-            t = torch.tensor([sms_], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            sms_ = t.item()
+        sms_ = max_over_ranks(sms_, dist, dev)
         s_ms = sms_ / args.steps
-        single = {"ms_per_step": s_ms, "value": world * T / (s_ms * 1e-3), "unit": UNIT,
+        single = {"ms_per_step": s_ms, "value": whole_job_rate(T, world, s_ms * 1e-3), "unit": UNIT,
                   "chunk_tokens": B.flce_forward_backward_chunk_tokens(T, H, V, dt_code),
                   "flops_per_step": roofline.flops(T, H, V, "model"),
                   "tensor_tflops": roofline.flops(T, H, V, "model") / (s_ms * 1e-3) / 1e12,
@@ -397,10 +408,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
         torch.cuda.synchronize(dev)
         _ = float(h_loss[0])
     e2e_s = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = t.item()
+    e2e_s = max_over_ranks(e2e_s, dist, dev)
     A.check_status(status)
     if rank != 0:
         return
@@ -430,7 +438,8 @@ def run_ours(args, wl, rank: int, world: int, dist):
         context = {"torch_eager": torch_eager_context(x, w, y)}
     pair_roles = B.flce_get_tuning(B.FLCE_TUNE_SM_PAIRS) if wl.dtype == "bf16" else 0
     out = {
-        "metric": METRIC, "value": world * T * args.steps / (total_ms * 1e-3), "unit": UNIT,
+        "metric": METRIC, "value": whole_job_rate(T * args.steps, world, total_ms * 1e-3),
+        "unit": UNIT,
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic: seeded PCG64, x~N(0,1), weight~N(0,0.02^2), targets %s" % wl.target_dist,
@@ -450,7 +459,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
                      "frac": achieved / peak_sus, "traffic": traffic,
                      "launches": n_launch, "peak_source": f"bf16_tflops_sustained of {peak_kind}"},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * T * e2e_steps / e2e_s, "unit": UNIT,
+        "e2e": {"value": whole_job_rate(T * e2e_steps, world, e2e_s), "unit": UNIT,
                 "h2d_bytes_per_step": int(hx.numel() * hx.element_size() +
                                           hw.numel() * hw.element_size() + hy.numel() * 8),
                 "d2h_bytes_per_step": 4},

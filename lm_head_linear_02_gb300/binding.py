@@ -19,7 +19,7 @@ __all__ = [
     "flce_forward_workspace_size", "flce_backward_workspace_size", "flce_backward_slab_width",
     "flce_set_backward_slab_width", "flce_forward", "flce_backward", "flce_strerror",
     "flce_forward_backward", "flce_forward_backward_workspace_size",
-    "flce_forward_backward_chunk_tokens",
+    "flce_forward_backward_chunk_tokens", "flce_test_withhold_signal",
     "flce_version", "flce_timing_enable", "flce_timing_read", "TIMING_ROLES",
     "flce_set_tuning", "flce_get_tuning", "FLCE_TUNE_RASTER_ROWS", "FLCE_TUNE_SM_PAIRS", "FLCE_ROLE_FORWARD", "FLCE_ROLE_DZ", "FLCE_ROLE_GRADS",
     "dtype_code", "reduction_code",
@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
     L.flce_get_tuning.restype = ci
     L.flce_set_tuning.argtypes = [ci, i64]
     L.flce_set_tuning.restype = ci
+    L.flce_test_withhold_signal.argtypes = []
+    L.flce_test_withhold_signal.restype = ci
     L.flce_strerror.argtypes = [ci]
     L.flce_strerror.restype = ctypes.c_char_p
     L.flce_version.argtypes = []
@@ -118,6 +120,11 @@ def _check(rc: int, where: str) -> int:
     if rc != FLCE_OK:
         raise FlceError(rc, where)
     return rc
+
+
+def flce_test_withhold_signal() -> None:
+    """Testing aid: the next single-SM contraction launch ends with FLCE_STATUS_TIMEOUT."""
+    _check(int(lib().flce_test_withhold_signal()), "flce_test_withhold_signal")
 
 
 def flce_strerror(code: int) -> str:

@@ -81,6 +81,12 @@ std::atomic<int> g_tune_sm_pairs{-1};
 }  // namespace
 
 int tune_raster_rows() { return g_tune_raster_rows.load(); }
+
+namespace {
+std::atomic<int> g_withhold_request{0};
+}  // namespace
+
+bool take_withhold_request() { return g_withhold_request.exchange(0) != 0; }
 int tune_sm_pairs() { return g_tune_sm_pairs.load(); }
 
 // ------------------------------------------------------------------------------- timing
@@ -356,6 +362,11 @@ int64_t flce_forward_backward_chunk_tokens(int64_t T, int64_t H, int64_t V, int 
 int64_t flce_backward_slab_width(int64_t T, int64_t H, int64_t V, int dtype) {
   if (!dims_ok(T, H, V, dtype)) return 0;
   return slab_width(T, V, dtype);
+}
+
+int flce_test_withhold_signal(void) {
+  flce::g_withhold_request.store(1);
+  return FLCE_OK;
 }
 
 int flce_timing_enable(int on) {

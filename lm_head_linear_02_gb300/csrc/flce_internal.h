@@ -23,6 +23,9 @@ constexpr int kTileN = 256;
 int tune_raster_rows();
 int tune_sm_pairs();
 
+// Consumes a pending flce_test_withhold_signal() request (true at most once per request).
+bool take_withhold_request();
+
 // Roles measured faster on CTA pairs, used by the automatic choice when every SM of the device
 // can be paired.
 constexpr int kAutoPairRoles = FLCE_ROLE_GRADS;

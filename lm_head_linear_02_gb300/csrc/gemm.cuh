@@ -46,6 +46,7 @@ struct GemmGrid {
   int* status;        // device status word (FLCE_STATUS_* bits)
   int* tile_counter;  // null: CTA b takes tiles b, b + grid, ...; else a zeroed device int that
                       // hands out tiles in list order to whichever CTA is free (dynamic)
+  int withhold;       // testing aid: CTA 0 does not signal its first accumulator tile
 };
 
 // Depth of the per-CTA queue through which the producer hands tile indices to the MMA thread
@@ -302,7 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));
+        // (g.withhold: the failure-path test leaves CTA 0's first tile unsignalled so that its
+        // epilogue's bounded wait runs out.)
+        if (!(g.withhold && blockIdx.x == 0 && consumed == k_blocks)) mma_commit(tfull_bar(acc));
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -415,6 +418,7 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& b0, const CUte
     e = cudaMemsetAsync(g.tile_counter, 0, sizeof(int), stream);
     if (e != cudaSuccess) return e;
   }
+  g.withhold = take_withhold_request() ? 1 : 0;
   const int grid = g.num_tiles < sms ? g.num_tiles : sms;
   kern<<<grid, kThreads, G::kSmemBytes, stream>>>(a0, b0, a1, b1, g, e0, e1);
   return cudaGetLastError();

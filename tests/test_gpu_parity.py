@@ -188,6 +188,29 @@ def test_out_of_range_target_sets_status_and_nan_loss():
         A.check_status(status)
 
 
+def test_pipeline_timeout_is_reported_and_device_stays_usable():
+    """A withheld pipeline signal ends the launch with FLCE_STATUS_TIMEOUT after the bounded wait
+    (about 2 s) instead of hanging; the next calls run normally on the same context."""
+    import time
+
+    inp = make_inputs("ragged", dtype="bf16")
+    x, w, y = to_device(inp)
+    B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, 0)  # the forward runs on the single-SM core
+    try:
+        B.flce_test_withhold_signal()
+        t0 = time.time()
+        loss, lse, status = A.flce_forward(x, w, y, "mean")
+        torch.cuda.synchronize()
+        waited = time.time() - t0
+        assert int(status.item()) & B.FLCE_STATUS_TIMEOUT
+        assert 1.0 < waited < 30.0
+        with pytest.raises(A.FlceDeviceError):
+            A.check_status(status)
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
+    assert_full_parity(inp, "mean", label="after timeout")
+
+
 def test_sum_mean_and_grad_loss_scaling():
     inp = make_inputs("ragged", dtype="bf16", T=512, seed=11)
     x, w, y = to_device(inp)
