@@ -719,7 +719,8 @@ int flce_forward_backward(const void* x, const void* weight, const int64_t* targ
   const auto DT = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const bool none = reduction == FLCE_REDUCTION_NONE;
   CUtensorMap tw_k, tw_mn;
-  if (!flce::make_tmap_2d(&tw_k, DT, weight, H, V, H * 2, 64, kTileN) ||
+  const uint32_t wbox = (flce::pair_roles(dev.sms) & FLCE_ROLE_FORWARD) ? 128 : kTileN;
+  if (!flce::make_tmap_2d(&tw_k, DT, weight, H, V, H * 2, 64, wbox) ||
       !flce::make_tmap_2d(&tw_mn, DT, weight, H, V, H * 2, 64, 64))
     return FLCE_ERR_CUDA;
 

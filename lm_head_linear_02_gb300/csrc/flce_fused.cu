@@ -57,10 +57,13 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
                                 const ChunkLaunch& c) {
   LogitsEpi::Args ea{c.target, c.part_m, c.part_s, c.zy, c.zbuf, c.ldz, c.rows, c.V};
+  const bool pairs = (pair_roles(c.sms) & FLCE_ROLE_FORWARD) != 0;  // W boxed {64 x 128} then
   GemmGrid g{};
-  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, kBM, 0);
+  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, pairs ? 256 : kBM, 0);
   g.num_problems = 1;
   g.status = c.status;
+  if (pairs)
+    return launch_pair<LogitsEpi, NoEpi>(tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{}, c.sms, c.stream);
   return launch_gemm<false, LogitsEpi, NoEpi>(tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{}, c.sms,
                                               c.stream);
 }

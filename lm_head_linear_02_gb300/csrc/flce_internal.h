@@ -27,8 +27,8 @@ int tune_sm_pairs();
 bool take_withhold_request();
 
 // Roles measured faster on CTA pairs, used by the automatic choice when every SM of the device
-// can be paired.
-constexpr int kAutoPairRoles = FLCE_ROLE_GRADS;
+// can be paired: the gradient launches (K = T or V, long tiles) and the forward projection.
+constexpr int kAutoPairRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_GRADS;
 
 // Effective FLCE_ROLE_* mask of bf16 roles that run on CTA pairs on the current device.
 int pair_roles(int sms);
@@ -153,7 +153,8 @@ struct ChunkLaunch {
   int sms;
   cudaStream_t stream;
 };
-// logits of the chunk: x_c K-major {64 x 128}, W K-major {64 x 256}
+// logits of the chunk: x_c K-major {64 x 128}, W K-major {64 x 256} ({64 x 128} when the forward
+// role runs on SM pairs)
 cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
                                 const ChunkLaunch& c);
 cudaError_t launch_form_dz(const ChunkLaunch& c);
