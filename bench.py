@@ -403,15 +403,22 @@ def run_ours(args, wl, rank: int, world: int, dist):
     h_loss = torch.empty(e2e_steps, dtype=torch.float32).pin_memory()
     copied = [torch.cuda.Event() for _ in range(e2e_steps)]
     done = [torch.cuda.Event() for _ in range(e2e_steps)]
+    # device-side spans of each step's copies and compute (diagnostics for the e2e line)
+    copy_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(e2e_steps)]
+    comp_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(e2e_steps)]
 
     def enqueue_copy(k):
         xb, wb, yb = bufs[k % 2]
         with torch.cuda.stream(copy_stream):
             if k >= 2:
                 copy_stream.wait_event(done[k - 2])
+            copy_ev[k][0].record(copy_stream)
             xb.copy_(hx, non_blocking=True)
             wb.copy_(hw, non_blocking=True)
             yb.copy_(hy, non_blocking=True)
+            copy_ev[k][1].record(copy_stream)
             copied[k].record(copy_stream)
 
     def run_step(xb, wb, yb):
@@ -422,6 +429,12 @@ def run_ours(args, wl, rank: int, world: int, dist):
                         dt_code, red, gl.data_ptr(), gx.data_ptr(), gw.data_ptr(), ws.data_ptr(),
                         bwd_ws, status.data_ptr(), sp)
 
+    # untimed warm-up of both input sets (first use of the second set's memory)
+    for xb, wb, yb in bufs:
+        xb.copy_(hx, non_blocking=True)
+        wb.copy_(hw, non_blocking=True)
+        yb.copy_(hy, non_blocking=True)
+        run_step(xb, wb, yb)
     barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -430,7 +443,9 @@ def run_ours(args, wl, rank: int, world: int, dist):
         if k + 1 < e2e_steps:
             enqueue_copy(k + 1)
         stream.wait_event(copied[k])
+        comp_ev[k][0].record(stream)
         run_step(*bufs[k % 2])
+        comp_ev[k][1].record(stream)
         h_loss[k].copy_(loss[0], non_blocking=True)
         done[k].record(stream)
     torch.cuda.synchronize(dev)
@@ -439,6 +454,8 @@ def run_ours(args, wl, rank: int, world: int, dist):
     e2e_s = max_over_ranks(e2e_s, dist, dev)
     if len(set(e2e_losses)) != 1:
         raise RuntimeError(f"end-to-end steps disagree: {e2e_losses}")
+    e2e_copy_ms = [a.elapsed_time(b) for a, b in copy_ev]
+    e2e_comp_ms = [a.elapsed_time(b) for a, b in comp_ev]
     del bufs
     A.check_status(status)
     if rank != 0:
@@ -492,6 +509,12 @@ def run_ours(args, wl, rank: int, world: int, dist):
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_rate(T * e2e_steps, world, e2e_s), "unit": UNIT,
                 "steps": e2e_steps, "overlap": "H2D of step k+1 on a copy stream during step k",
+                "wall_ms_per_step": e2e_s * 1e3 / e2e_steps,
+                "copy_ms_per_step": statistics.median(e2e_copy_ms),
+                "compute_ms_per_step": statistics.median(e2e_comp_ms),
+                "compute_ms_steps": [round(v, 3) for v in e2e_comp_ms],
+                "gap_ms_steps": [round(comp_ev[k][1].elapsed_time(comp_ev[k + 1][0]), 3)
+                                 for k in range(e2e_steps - 1)],
                 "h2d_bytes_per_step": int(hx.numel() * hx.element_size() +
                                           hw.numel() * hw.element_size() + hy.numel() * 8),
                 "d2h_bytes_per_step": 4},

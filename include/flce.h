@@ -201,9 +201,16 @@ int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_RO
  *                          picks a measured mask when every SM of the current device can be
  *                          given a partner at once and 0 otherwise (how many pairs fit depends
  *                          on how a chip's SMs are grouped, not only on their number).
+ *   FLCE_TUNE_WIDE_TILES   which of the roles on SM pairs use wide tiles: each CTA stages 256
+ *                          rows of the A operand and issues two MMAs per K step (512 x 256 pair
+ *                          tiles), which needs 25% less shared-memory fill per FLOP than the
+ *                          128-row CTA tiles but leaves no TMEM for overlapping a tile's
+ *                          epilogue with the next tile. A bit mask of FLCE_ROLE_*; -1 (the
+ *                          default) picks a measured mask. Roles not on SM pairs ignore it.
  * Read at each launch. Returns FLCE_OK or FLCE_ERR_ARG. */
 #define FLCE_TUNE_RASTER_ROWS 1
 #define FLCE_TUNE_SM_PAIRS 2
+#define FLCE_TUNE_WIDE_TILES 3
 #define FLCE_ROLE_FORWARD 1
 #define FLCE_ROLE_DZ 2
 #define FLCE_ROLE_GRADS 4

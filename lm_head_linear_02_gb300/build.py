@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libflce.so")
 SOURCES = ("flce_fwd.cu", "flce_bwd.cu", "flce_fused.cu", "flce_abi.cu", "flce_static_scratch.cu")
-HEADERS = ("ptx.cuh", "gemm.cuh", "epilogues.cuh", "flce_internal.h")
+HEADERS = tuple(sorted(f for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))))
 ARCH = ("-gencode", "arch=compute_103a,code=sm_103a")
 CFLAGS = ("-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr")

@@ -78,6 +78,7 @@ bool make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uin
 namespace {
 std::atomic<int> g_tune_raster_rows{2048};
 std::atomic<int> g_tune_sm_pairs{-1};
+std::atomic<int> g_tune_wide_tiles{-1};
 }  // namespace
 
 int tune_raster_rows() { return g_tune_raster_rows.load(); }
@@ -88,6 +89,7 @@ std::atomic<int> g_withhold_request{0};
 
 bool take_withhold_request() { return g_withhold_request.exchange(0) != 0; }
 int tune_sm_pairs() { return g_tune_sm_pairs.load(); }
+int tune_wide_tiles() { return g_tune_wide_tiles.load(); }
 
 // ------------------------------------------------------------------------------- timing
 // Optional event brackets around each contraction launch (see flce_timing_enable).
@@ -417,6 +419,10 @@ int flce_set_tuning(int key, int64_t value) {
       if (value < -1 || value > 7) return FLCE_ERR_ARG;
       flce::g_tune_sm_pairs.store(static_cast<int>(value));
       return FLCE_OK;
+    case FLCE_TUNE_WIDE_TILES:
+      if (value < -1 || value > 7) return FLCE_ERR_ARG;
+      flce::g_tune_wide_tiles.store(static_cast<int>(value));
+      return FLCE_OK;
     default:
       return FLCE_ERR_ARG;
   }
@@ -432,6 +438,11 @@ int flce_get_tuning(int key, int64_t* value) {
       flce::Device dev;
       if (!flce::current_device(&dev)) return FLCE_ERR_CUDA;
       *value = flce::pair_roles(dev.sms);
+      return FLCE_OK;
+    }
+    case FLCE_TUNE_WIDE_TILES: {
+      const int w = flce::tune_wide_tiles();
+      *value = w >= 0 ? w : flce::kDefaultWideRoles;
       return FLCE_OK;
     }
     default:
@@ -500,9 +511,11 @@ int flce_forward(const void* x, const void* weight, const int64_t* target, int64
   cudaError_t e;
   if (dtype == FLCE_DTYPE_BF16) {
     CUtensorMap tx, tw;
-    if (!flce::make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, H, T, H * 2, 64, kTileM) ||
+    const flce::Core core = flce::role_core(dev.sms, FLCE_ROLE_FORWARD);
+    if (!flce::make_tmap_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, H, T, H * 2, 64,
+                            flce::core_a_box_rows(core)) ||
         !flce::make_tmap_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, weight, H, V, H * 2, 64,
-                            (flce::pair_roles(dev.sms) & FLCE_ROLE_FORWARD) ? 128 : kTileN))
+                            flce::core_b_box_rows(core)))
       return FLCE_ERR_CUDA;
     e = flce::timed_launch(0, s, [&] { return flce::launch_forward_bf16(tx, tw, p); });
   } else {
@@ -570,7 +583,8 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
   // Slab-invariant operand maps.
   CUtensorMap tx, tx_mn, txh, txl, txth, txtl;
   if (bf16) {
-    if (!flce::make_tmap_2d(&tx, DT, x, H, T, H * 2, bk, kTileM) ||
+    if (!flce::make_tmap_2d(&tx, DT, x, H, T, H * 2, bk,
+                            flce::core_a_box_rows(flce::role_core(dev.sms, FLCE_ROLE_DZ))) ||
         !flce::make_tmap_2d(&tx_mn, DT, x, H, T, H * 2, 64, 64))
       return FLCE_ERR_CUDA;
   } else {
@@ -639,10 +653,11 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
     if (bf16) {
       const uint8_t* wslab = static_cast<const uint8_t*>(weight) + size_t(slab0) * H * 2;
       CUtensorMap tws, tdz_mn, tdz_k, tw_mn;
-      const uint32_t wbox = (flce::pair_roles(dev.sms) & FLCE_ROLE_DZ) ? 128 : kTileN;
+      const uint32_t wbox = flce::core_b_box_rows(flce::role_core(dev.sms, FLCE_ROLE_DZ));
+      const uint32_t dzbox = flce::core_a_box_rows(flce::role_core(dev.sms, FLCE_ROLE_GRADS));
       if (!flce::make_tmap_2d(&tws, DT, wslab, H, sw, H * 2, bk, wbox) ||
           !flce::make_tmap_2d(&tdz_mn, DT, w.dz, sw, T, w.vc * 2, 64, 64) ||
-          !flce::make_tmap_2d(&tdz_k, DT, w.dz, sw, T, w.vc * 2, bk, kTileM) ||
+          !flce::make_tmap_2d(&tdz_k, DT, w.dz, sw, T, w.vc * 2, bk, dzbox) ||
           !flce::make_tmap_2d(&tw_mn, DT, wslab, H, sw, H * 2, 64, 64))
         return FLCE_ERR_CUDA;
       e = flce::timed_launch(1, s, [&] { return flce::launch_dz_bf16(tx, tws, dz); });
@@ -719,8 +734,9 @@ int flce_forward_backward(const void* x, const void* weight, const int64_t* targ
   const auto DT = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const bool none = reduction == FLCE_REDUCTION_NONE;
   CUtensorMap tw_k, tw_mn;
-  const uint32_t wbox = (flce::pair_roles(dev.sms) & FLCE_ROLE_FORWARD) ? 128 : kTileN;
-  if (!flce::make_tmap_2d(&tw_k, DT, weight, H, V, H * 2, 64, wbox) ||
+  const flce::Core fcore = flce::role_core(dev.sms, FLCE_ROLE_FORWARD);
+  const flce::Core gcore = flce::role_core(dev.sms, FLCE_ROLE_GRADS);
+  if (!flce::make_tmap_2d(&tw_k, DT, weight, H, V, H * 2, 64, flce::core_b_box_rows(fcore)) ||
       !flce::make_tmap_2d(&tw_mn, DT, weight, H, V, H * 2, 64, 64))
     return FLCE_ERR_CUDA;
 
@@ -730,9 +746,10 @@ int flce_forward_backward(const void* x, const void* weight, const int64_t* targ
     const int64_t rows = (T - t0) < w.rows ? (T - t0) : w.rows;
     const uint8_t* xc = static_cast<const uint8_t*>(x) + size_t(t0) * H * 2;
     CUtensorMap tx_k, tx_mn, tz_k, tz_mn;
-    if (!flce::make_tmap_2d(&tx_k, DT, xc, H, rows, H * 2, 64, kTileM) ||
+    if (!flce::make_tmap_2d(&tx_k, DT, xc, H, rows, H * 2, 64, flce::core_a_box_rows(fcore)) ||
         !flce::make_tmap_2d(&tx_mn, DT, xc, H, rows, H * 2, 64, 64) ||
-        !flce::make_tmap_2d(&tz_k, DT, w.zbuf, V, rows, w.ldz * 2, 64, kTileM) ||
+        !flce::make_tmap_2d(&tz_k, DT, w.zbuf, V, rows, w.ldz * 2, 64,
+                            flce::core_a_box_rows(gcore)) ||
         !flce::make_tmap_2d(&tz_mn, DT, w.zbuf, V, rows, w.ldz * 2, 64, 64))
       return FLCE_ERR_CUDA;
     flce::ChunkLaunch cl{};

@@ -24,13 +24,14 @@ static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const 
 cudaError_t launch_dz_bf16(const CUtensorMap& tx, const CUtensorMap& tw_slab, const DzLaunch& p) {
   typename DzEpi<false>::Args ea{p.target, p.lse, p.row_scale, p.dz, nullptr, nullptr, nullptr,
                                  p.ldz,    p.ldt, p.T,         p.slab0, p.slab_w};
-  if (pair_roles(p.sms) & FLCE_ROLE_DZ) {  // W slab map boxed {64 x 128} for this path
+  const Core core = role_core(p.sms, FLCE_ROLE_DZ);
+  if (core != kCoreSingle) {  // x boxed {64 x core_a_box_rows}, W slab {64 x 128} for this path
     GemmGrid g{};
-    g.p[0] = make_problem(p.T, p.slab_w, p.H, 64, false, false, 256, 0);
+    g.p[0] = make_problem(p.T, p.slab_w, p.H, 64, false, false, core_tile_rows(core), 0);
     g.num_problems = 1;
     g.status = p.status;
-    return launch_pair<DzEpi<false>, NoEpi>(tx, tw_slab, tx, tw_slab, g, ea, NoEpi::Args{}, p.sms,
-                                            p.stream);
+    return launch_pair_core<DzEpi<false>, NoEpi>(core, tx, tw_slab, tx, tw_slab, g, ea,
+                                                 NoEpi::Args{}, p.sms, p.stream);
   }
   return run_gemm<false, DzEpi<false>>(tx, tw_slab, tx, tw_slab, p.T, p.slab_w, p.H, p.status,
                                        p.sms, p.stream, ea);
@@ -65,16 +66,16 @@ cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
   typename GradWEpi<false>::Args ew{pw.grad_w, pw.grad_loss, pw.scale, pw.H, pw.slab0, pw.slab_w};
   typename GradXEpi<false>::Args ex{px.acc,   px.grad_x, px.grad_loss, px.scale,
                                     px.T,     px.H,      px.mode};
-  const bool pairs = (pair_roles(pw.sms) & FLCE_ROLE_GRADS) != 0;
-  const int rows = pairs ? 256 : kBM;
+  const Core core = role_core(pw.sms, FLCE_ROLE_GRADS);  // dz K-major map boxed to match
+  const int rows = core_tile_rows(core);
   GemmGrid g{};
   g.p[0] = make_problem(pw.slab_w, pw.H, pw.T, 64, true, true, rows, 0);
   g.p[1] = make_problem(px.T, px.H, px.K, 64, false, true, rows, g.p[0].m_tiles * g.p[0].n_tiles);
   g.num_problems = 2;
   g.status = pw.status;
-  if (pairs)
-    return launch_pair<GradWEpi<false>, GradXEpi<false>>(tdz_mn, tx_mn, tdz_k, tw_mn, g, ew, ex,
-                                                         pw.sms, pw.stream);
+  if (core != kCoreSingle)
+    return launch_pair_core<GradWEpi<false>, GradXEpi<false>>(core, tdz_mn, tx_mn, tdz_k, tw_mn, g,
+                                                              ew, ex, pw.sms, pw.stream);
   return launch_gemm<false, GradWEpi<false>, GradXEpi<false>>(tdz_mn, tx_mn, tdz_k, tw_mn, g, ew,
                                                               ex, pw.sms, pw.stream);
 }
@@ -82,13 +83,13 @@ cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
 int pair_roles(int sms) {
   const int t = tune_sm_pairs();
   if (t >= 0) return t;
-  auto kern = k_umma_gemm_pair<GradWEpi<false>, GradXEpi<false>>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes) !=
-      cudaSuccess) {
+  auto kern = k_umma_gemm_pair<128, GradWEpi<false>, GradXEpi<false>>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PairGeom<128>::kSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  return 2 * pair_resident_clusters(kern, sms) >= 2 * (sms / 2) ? kAutoPairRoles : 0;
+  return 2 * pair_resident_clusters<128>(kern, sms) >= 2 * (sms / 2) ? kAutoPairRoles : 0;
 }
 
 cudaError_t launch_gradw_tf32(const CUtensorMap& tdzt_hi, const CUtensorMap& txt_hi,

@@ -57,13 +57,14 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
                                 const ChunkLaunch& c) {
   LogitsEpi::Args ea{c.target, c.part_m, c.part_s, c.zy, c.zbuf, c.ldz, c.rows, c.V};
-  const bool pairs = (pair_roles(c.sms) & FLCE_ROLE_FORWARD) != 0;  // W boxed {64 x 128} then
+  const Core core = role_core(c.sms, FLCE_ROLE_FORWARD);  // maps boxed for this core
   GemmGrid g{};
-  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, pairs ? 256 : kBM, 0);
+  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, core_tile_rows(core), 0);
   g.num_problems = 1;
   g.status = c.status;
-  if (pairs)
-    return launch_pair<LogitsEpi, NoEpi>(tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{}, c.sms, c.stream);
+  if (core != kCoreSingle)
+    return launch_pair_core<LogitsEpi, NoEpi>(core, tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{}, c.sms,
+                                              c.stream);
   return launch_gemm<false, LogitsEpi, NoEpi>(tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{}, c.sms,
                                               c.stream);
 }
@@ -87,8 +88,8 @@ cudaError_t launch_chunk_grads(const CUtensorMap& tz_k, const CUtensorMap& tw_mn
                                     c.rows,  c.H,           0};
   typename GradXEpi<false>::Args ew{c.gw_acc, c.grad_w, c.grad_loss, c.scale,
                                     c.V,      c.H,      c.gw_mode};
-  const bool pairs = (pair_roles(c.sms) & FLCE_ROLE_GRADS) != 0;
-  const int tile_rows = pairs ? 256 : kBM;
+  const Core core = role_core(c.sms, FLCE_ROLE_GRADS);  // zbuf K-major map boxed to match
+  const int tile_rows = core_tile_rows(core);
   GemmGrid g{};
   g.p[0] = make_problem(c.rows, c.H, c.V, 64, false, true, tile_rows, 0);
   g.p[1] = make_problem(c.V, c.H, c.rows, 64, true, true, tile_rows,
@@ -96,9 +97,9 @@ cudaError_t launch_chunk_grads(const CUtensorMap& tz_k, const CUtensorMap& tw_mn
   g.num_problems = 2;
   g.status = c.status;
   g.tile_counter = c.tile_counter;
-  if (pairs)
-    return launch_pair<GradXEpi<false>, GradXEpi<false>>(tz_k, tw_mn, tz_mn, tx_mn, g, ex, ew, c.sms,
-                                                         c.stream);
+  if (core != kCoreSingle)
+    return launch_pair_core<GradXEpi<false>, GradXEpi<false>>(core, tz_k, tw_mn, tz_mn, tx_mn, g, ex,
+                                                              ew, c.sms, c.stream);
   return launch_gemm<false, GradXEpi<false>, GradXEpi<false>>(tz_k, tw_mn, tz_mn, tx_mn, g, ex, ew,
                                                               c.sms, c.stream);
 }

@@ -122,14 +122,15 @@ cudaError_t launch_finalize(const float* block_sums, int n_blocks, int T, int re
 }
 
 cudaError_t launch_forward_bf16(const CUtensorMap& tx, const CUtensorMap& tw, const FwdLaunch& p) {
-  if (pair_roles(p.sms) & FLCE_ROLE_FORWARD) {  // W map boxed {64 x 128} for this path
+  const Core core = role_core(p.sms, FLCE_ROLE_FORWARD);
+  if (core != kCoreSingle) {  // x boxed {64 x core_a_box_rows}, W {64 x 128} for this path
     GemmGrid g{};
-    g.p[0] = make_problem(p.T, p.V, p.H, 64, false, false, 256, 0);
+    g.p[0] = make_problem(p.T, p.V, p.H, 64, false, false, core_tile_rows(core), 0);
     g.num_problems = 1;
     g.status = p.status;
     FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V};
-    cudaError_t e = launch_pair<FwdEpi, NoEpi>(tx, tw, tx, tw, g, ea, NoEpi::Args{}, p.sms,
-                                               p.stream);
+    cudaError_t e = launch_pair_core<FwdEpi, NoEpi>(core, tx, tw, tx, tw, g, ea, NoEpi::Args{},
+                                                    p.sms, p.stream);
     if (e != cudaSuccess) return e;
     return launch_combine(p);
   }

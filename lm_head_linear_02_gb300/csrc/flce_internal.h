@@ -20,18 +20,40 @@ constexpr int kTileN = 256;
 //                       so the group's A rows stay in L2 while B streams); default 2048.
 //   tune_sm_pairs():    bit mask of the bf16 roles (FLCE_ROLE_*) that run on CTA pairs, or -1
 //                       (the default) to decide per device.
+//   tune_wide_tiles(): bit mask of the roles whose CTA pairs use 256-row CTA tiles, or -1 (the
+//                      default: kDefaultWideRoles).
 int tune_raster_rows();
 int tune_sm_pairs();
+int tune_wide_tiles();
 
 // Consumes a pending flce_test_withhold_signal() request (true at most once per request).
 bool take_withhold_request();
 
 // Roles measured faster on CTA pairs, used by the automatic choice when every SM of the device
-// can be paired: the gradient launches (K = T or V, long tiles) and the forward projection.
-constexpr int kAutoPairRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_GRADS;
+// can be paired: all three (with the wide CTA tiles below; on 128-row CTA tiles dz alone was
+// faster on single SMs).
+constexpr int kAutoPairRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ | FLCE_ROLE_GRADS;
+
+// Roles measured faster on 256-row CTA tiles when they run on CTA pairs.
+constexpr int kDefaultWideRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ | FLCE_ROLE_GRADS;
 
 // Effective FLCE_ROLE_* mask of bf16 roles that run on CTA pairs on the current device.
 int pair_roles(int sms);
+
+// The contraction core a bf16 role launches on: single-SM 128 x 256 tiles, CTA pairs with
+// 128-row CTA tiles (256 x 256 pair tiles) or CTA pairs with 256-row CTA tiles (512 x 256).
+enum Core { kCoreSingle = 0, kCorePair = 1, kCoreWide = 2 };
+inline Core role_core(int sms, int role) {
+  if ((pair_roles(sms) & role) == 0) return kCoreSingle;
+  const int w = tune_wide_tiles();
+  return ((w >= 0 ? w : kDefaultWideRoles) & role) ? kCoreWide : kCorePair;
+}
+// M rows of one tile (GemmProblem tile_rows) on a core.
+inline int core_tile_rows(Core c) { return c == kCoreWide ? 512 : c == kCorePair ? 256 : 128; }
+// Rows of the box of a K-major A operand map ({64 x rows}) on a core.
+inline uint32_t core_a_box_rows(Core c) { return c == kCoreWide ? 256u : 128u; }
+// Rows of the box of a K-major B operand map ({64 x rows}): one CTA's N half on pairs.
+inline uint32_t core_b_box_rows(Core c) { return c == kCoreSingle ? 256u : 128u; }
 
 struct Device {
   int id = -1;

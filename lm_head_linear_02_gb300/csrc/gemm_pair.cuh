@@ -1,19 +1,28 @@
 // gemm_pair.cuh - the bf16 contraction core on CTA pairs (tcgen05 cta_group::2).
 //
-// A cluster of two CTAs on two SMs computes one 256 x 256 output tile with one MMA stream: CTA
-// r holds rows [128r, 128r + 128) of the A tile and rows [128r, 128r + 128) of the B tile (the
-// N dimension), the pair's tensor cores exchange the B halves, and CTA r's TMEM receives its 128
-// rows of D across all 256 columns. Per SM this halves the B operand that must be staged in
-// shared memory, so a 64-deep K slice costs 32 KB per CTA instead of 48 KB: six pipeline stages
-// fit where the single-CTA core holds four, and L2 -> SM traffic per FLOP drops by a third.
+// A cluster of two CTAs on two SMs computes one (2 kRows) x 256 output tile with one MMA stream:
+// CTA r holds rows [kRows r, kRows r + kRows) of the A tile and rows [128r, 128r + 128) of the
+// B tile (the N dimension), the pair's tensor cores exchange the B halves, and CTA r's TMEM
+// receives its kRows rows of D across all 256 columns. Two geometries:
+//   kRows = 128: 256 x 256 pair tiles; a 64-deep K slice costs 32 KB per CTA (16 KB of A, 16 KB
+//                of B), six pipeline stages, two 256-column accumulators (the epilogue of one
+//                tile overlaps the main loop of the next).
+//   kRows = 256: 512 x 256 pair tiles; each K step issues two M=256 MMAs (the CTA's two 128-row
+//                halves of A against the same B), so a K slice costs 48 KB per CTA for twice the
+//                FLOPs: 48 instead of 64 bytes of shared-memory fill per 1024 FLOPs. On GB300 the
+//                TMA fill rate of one SM, not the tensor core, bounds the 128-row geometry (about
+//                40-50 B per SM clock measured, 64 needed), so this one keeps the tensor pipe
+//                busy; the price is one accumulator filling all 512 TMEM columns, so the epilogue
+//                of a tile is not hidden behind the next main loop (8 epilogue warps halve it).
 //
-// Roles (6 warps per CTA, as in gemm.cuh):
-//   warp 0 (both CTAs)   TMA producer: loads this CTA's A and B halves; completion is counted
-//                        on the LEADER's full barrier, which the leader arms for both halves.
-//   warp 1 (leader)      MMA issuer: waits for both halves, issues M=256 N=256 MMAs, and
+// Roles (per CTA: 2 + 4 kRows / 128 warps):
+//   warp 0 (both CTAs)   TMA producer: loads this CTA's A rows and B half; completion is counted
+//                        on the LEADER's full barrier, which the leader arms for both CTAs.
+//   warp 1 (leader)      MMA issuer: waits for both CTAs' bytes, issues M=256 N=256 MMAs, and
 //                        commits to the empty / tmem-full barriers of BOTH CTAs (multicast).
 //   warp 1 (peer)        idle (takes part in the pair's TMEM allocation only).
-//   warps 2..5 (both)    epilogue: drain this CTA's 128 accumulator rows, then tell the
+//   warps 2.. (both)     epilogue: warp 2 + 4h + q drains TMEM lanes [32q', 32q' + 32) of half h
+//                        (q' = warp % 4, the lane quarter a warp may access), then tells the
 //                        leader (remote mbarrier arrive) that the accumulator is free.
 // A launch may carry two independent problems: grad_W and grad_x of one vocab slab run together,
 // so that their tiles fill the GPU in one wave pattern instead of two.
@@ -23,23 +32,37 @@
 
 namespace flce {
 
-constexpr int kPairStages = 6;
-constexpr uint32_t kPairABytes = 128 * 128;  // 128 rows x 64 bf16
-constexpr uint32_t kPairBBytes = 128 * 128;  // this CTA's 128 N rows x 64 bf16
-constexpr uint32_t kPairStageBytes = kPairABytes + kPairBBytes;
-constexpr uint32_t kPairRingBytes = kPairStages * kPairStageBytes;
-constexpr uint32_t kPairSmemBytes = kPairRingBytes + 1024 + 1024;
+template <int kRows>
+struct PairGeom {
+  static_assert(kRows == 128 || kRows == 256, "rows per CTA: 128 or 256");
+  static constexpr int kHalves = kRows / 128;          // M=256 MMAs per K step / epilogue halves
+  static constexpr int kStages = kRows == 128 ? 6 : 4;
+  static constexpr uint32_t kABytes = kRows * 128;     // kRows rows x 64 bf16
+  static constexpr uint32_t kBBytes = 128 * 128;       // this CTA's 128 N rows x 64 bf16
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kRingBytes = kStages * kStageBytes;
+  static constexpr uint32_t kSmemBytes = kRingBytes + 1024 + 1024;
+  static constexpr int kAccBufs = 2 / kHalves;         // accumulators in the 512 TMEM columns
+  static constexpr int kEpiWarps = 4 * kHalves;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kTileRows = 2 * kRows;          // M rows of one pair tile
+};
 constexpr int kPairBK = 64;
 
-// Tiles are 256 x 256 here: GemmProblem::m_tiles counts 256-row tiles (make_problem with
-// tile_rows = 256) and the epilogue receives 128-row block indices (2 * mb + rank).
-template <class Epi0, class Epi1>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// GemmProblem::m_tiles counts pair tiles of 2 kRows rows (make_problem with tile_rows =
+// PairGeom<kRows>::kTileRows) and the epilogue receives 128-row block indices.
+template <int kRows, class Epi0, class Epi1>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kThreads, 1)
     k_umma_gemm_pair(const __grid_constant__ CUtensorMap tA0,
                      const __grid_constant__ CUtensorMap tB0,
                      const __grid_constant__ CUtensorMap tA1,
                      const __grid_constant__ CUtensorMap tB1, const GemmGrid g,
                      const typename Epi0::Args e0, const typename Epi1::Args e1) {
+  using G = PairGeom<kRows>;
+  constexpr int kPairStages = G::kStages;
+  constexpr uint32_t kPairABytes = G::kABytes;
+  constexpr uint32_t kPairStageBytes = G::kStageBytes;
+  constexpr uint32_t kPairRingBytes = G::kRingBytes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -69,7 +92,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // Tile indices flow through a small queue in each CTA: the leader's producer takes the next
   // tile (fixed stride or the shared counter) and writes it into both CTAs' queues; the
   // leader's MMA thread, the peer's producer and the epilogue warps of both CTAs read it and
-  // release the slot back to the leader (1 + 1 + 4 + 4 = 10 arrivals).
+  // release the slot back to the leader (1 + 1 + 2 kEpiWarps arrivals).
   auto tq_release = [&](int q) {
     if (leader)
       mbar_arrive(tq_empty(q));
@@ -84,12 +107,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 8);  // leader: 4 epilogue warps x 2 CTAs
+      mbar_init(tempty_bar(a), 2 * G::kEpiWarps);  // leader: every epilogue warp of both CTAs
     }
     mbar_init(drain_bar(), 1);
     for (int q = 0; q < kTileQueue; ++q) {
       mbar_init(tq_full(q), 1);
-      mbar_init(tq_empty(q), 10);
+      mbar_init(tq_empty(q), 2 + 2 * G::kEpiWarps);
     }
     *abort_flag = 0;
     *issued_fills = 0;
@@ -148,7 +171,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const TileInfo pt = map_tile(g, t);
         const CUtensorMap* ta = pt.prob ? &tA1 : &tA0;
         const CUtensorMap* tb = pt.prob ? &tB1 : &tB0;
-        const int m0 = pt.mb * 256 + static_cast<int>(rank) * 128;
+        const int m0 = pt.mb * G::kTileRows + static_cast<int>(rank) * kRows;
         const int n0 = pt.nb * 256 + static_cast<int>(rank) * 128;
         const bool a_mn = pt.a_mn != 0, b_mn = pt.b_mn != 0;
         const int k_blocks = pt.k_blocks;
@@ -162,11 +185,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t sA = ring + stage * kPairStageBytes;
           const uint32_t sB = sA + kPairABytes;
           const int k0 = kb * kPairBK;
-          if (!a_mn) {
+          if (!a_mn) {  // one box of kRows rows (the A map is boxed {64 x kRows})
             tma_load_2d_pair(sA, ta, fb, k0, m0);
-          } else {
-            tma_load_2d_pair(sA, ta, fb, m0, k0);
-            tma_load_2d_pair(sA + 8192u, ta, fb, m0 + 64, k0);
+          } else {  // kRows / 64 boxes of {64 (M) x 64 (K)}
+#pragma unroll
+            for (int j = 0; j < kRows / 64; ++j)
+              tma_load_2d_pair(sA + 8192u * j, ta, fb, m0 + 64 * j, k0);
           }
           if (!b_mn) {
             tma_load_2d_pair(sB, tb, fb, k0, n0);
@@ -219,7 +243,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // Accumulator handshake with both CTAs' epilogues: cluster-scope acquire.
         if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, g.status, abort_flag)) break;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * G::kHalves * kBN);
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, g.status, abort_flag)) {
             ok = false;
@@ -228,9 +252,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tc_fence_after_sync();
           const uint64_t soff = static_cast<uint64_t>(stage * kPairStageBytes) >> 4;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_pair(d_tmem, a_base + soff + kk * a_step, b_base + soff + kk * b_step, idesc,
-                          (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+            for (int h = 0; h < G::kHalves; ++h)  // half h: A rows [128h, 128h + 128), +16 KB
+              mma_bf16_pair(d_tmem + static_cast<uint32_t>(h * kBN),
+                            a_base + soff + h * (16384u >> 4) + kk * a_step,
+                            b_base + soff + kk * b_step, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
           mma_commit_pair(empty_bar(stage), 0x3);
           ++consumed;
           if (++stage == kPairStages) {
@@ -240,7 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit_pair(tfull_bar(acc), 0x3);
-        if (++acc == 2) {
+        if (++acc == G::kAccBufs) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -251,6 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------------ epilogue (both CTAs)
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -274,8 +303,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       __syncwarp();
       const TileInfo pt = map_tile(g, t);
-      const int mb128 = pt.mb * 2 + static_cast<int>(rank);
-      const uint32_t taddr = tmem_base + static_cast<uint32_t>(acc * kBN) +
+      const int mb128 = (pt.mb * 2 + static_cast<int>(rank)) * G::kHalves + half;
+      const uint32_t taddr = tmem_base + static_cast<uint32_t>((acc * G::kHalves + half) * kBN) +
                              (static_cast<uint32_t>(quarter * 32) << 16);
       if (pt.prob == 0)
         Epi0::tile(e0, st0, mb128, pt.nb, row, taddr);
@@ -284,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
-      if (++acc == 2) {
+      if (++acc == G::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -327,16 +356,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // How many CTA pairs of `kern` can be resident at once on the current device (queried once
 // per device and kernel). Depends on how the chip's SMs are grouped, not only on their count.
-template <class K>
+template <int kRows, class K>
 int pair_resident_clusters(K kern, int sms) {
+  using G = PairGeom<kRows>;
   static int cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return sms / 2;
   if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.blockDim = dim3(G::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = G::kSmemBytes;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
     cudaGetLastError();  // clear the query's error; fall back to one pair per two SMs
@@ -347,24 +377,37 @@ int pair_resident_clusters(K kern, int sms) {
 }
 
 // Launch one or two problems on CTA pairs: a persistent grid of as many pairs as can be
-// resident at once (at most one per tile).
-template <class Epi0, class Epi1>
+// resident at once (at most one per tile). The problems' m_tiles count PairGeom<kRows>::
+// kTileRows-row tiles, and K-major A operands are boxed {64 x kRows}.
+template <int kRows, class Epi0, class Epi1>
 cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
                         const CUtensorMap& b1, GemmGrid g, const typename Epi0::Args& e0,
                         const typename Epi1::Args& e1, int sms, cudaStream_t stream) {
-  auto kern = k_umma_gemm_pair<Epi0, Epi1>;
+  using G = PairGeom<kRows>;
+  auto kern = k_umma_gemm_pair<kRows, Epi0, Epi1>;
   cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmemBytes);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int max_clusters = pair_resident_clusters(kern, sms);
+  const int max_clusters = pair_resident_clusters<kRows>(kern, sms);
   finish_grid(g);
   if (g.tile_counter) {
     e = cudaMemsetAsync(g.tile_counter, 0, sizeof(int), stream);
     if (e != cudaSuccess) return e;
   }
   const int clusters = g.num_tiles < max_clusters ? g.num_tiles : max_clusters;
-  kern<<<2 * clusters, kThreads, kPairSmemBytes, stream>>>(a0, b0, a1, b1, g, e0, e1);
+  kern<<<2 * clusters, G::kThreads, G::kSmemBytes, stream>>>(a0, b0, a1, b1, g, e0, e1);
   return cudaGetLastError();
+}
+
+// Launch on a pair core (kCorePair: 128-row CTA tiles, kCoreWide: 256-row CTA tiles); the
+// problems must have been made with core_tile_rows(core).
+template <class Epi0, class Epi1>
+cudaError_t launch_pair_core(Core core, const CUtensorMap& a0, const CUtensorMap& b0,
+                             const CUtensorMap& a1, const CUtensorMap& b1, GemmGrid g,
+                             const typename Epi0::Args& e0, const typename Epi1::Args& e1, int sms,
+                             cudaStream_t stream) {
+  if (core == kCoreWide) return launch_pair<256, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
+  return launch_pair<128, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
 }
 
 }  // namespace flce

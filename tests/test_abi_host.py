@@ -160,7 +160,8 @@ def test_binding_raises_on_error(lib):
 def test_tuning_knobs_validate(lib):
     assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_ROWS) == 2048
     for key, bad in [(B.FLCE_TUNE_RASTER_ROWS, 100), (B.FLCE_TUNE_RASTER_ROWS, 0),
-                     (B.FLCE_TUNE_SM_PAIRS, 8), (B.FLCE_TUNE_SM_PAIRS, -2), (99, 1)]:
+                     (B.FLCE_TUNE_SM_PAIRS, 8), (B.FLCE_TUNE_SM_PAIRS, -2),
+                     (B.FLCE_TUNE_WIDE_TILES, 8), (B.FLCE_TUNE_WIDE_TILES, -2), (99, 1)]:
         with pytest.raises(B.FlceError):
             B.flce_set_tuning(key, bad)
     B.flce_set_tuning(B.FLCE_TUNE_RASTER_ROWS, 4096)
@@ -168,3 +169,11 @@ def test_tuning_knobs_validate(lib):
         assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_ROWS) == 4096
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_RASTER_ROWS, 2048)
+    # the wide-tile mask needs no device to report: default (all roles) or the value set
+    assert B.flce_get_tuning(B.FLCE_TUNE_WIDE_TILES) == 7
+    B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, 5)
+    try:
+        assert B.flce_get_tuning(B.FLCE_TUNE_WIDE_TILES) == 5
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
+    assert B.flce_get_tuning(B.FLCE_TUNE_WIDE_TILES) == 7

@@ -134,20 +134,52 @@ def test_parity_reduction_none(name, dtype):
     assert e_loss <= tol["loss"] and e_gx <= tol["grad"] and e_gw <= tol["grad"]
 
 
-@pytest.mark.parametrize("pair", [0, 7])
-def test_parity_single_sm_and_sm_pair_tiles(pair):
-    """Every bf16 role on single-SM tiles (0) and on SM pairs (7), several slabs, ragged shapes."""
+@pytest.mark.parametrize("pair,wide", [(0, 0), (7, 0), (7, 7), (7, 2)])
+def test_parity_single_sm_and_sm_pair_tiles(pair, wide):
+    """Every bf16 role on single-SM tiles (pair 0), on SM pairs with 128-row CTA tiles (wide 0)
+    and with 256-row CTA tiles (wide 7: all roles; wide 2: dz only, so that one launch's
+    operand maps are boxed for a different core than the next one's), several slabs, ragged
+    shapes (token counts far from a multiple of the 512-row wide tile)."""
     B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
+    B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
     B.flce_set_backward_slab_width(2048)
     try:
         assert B.flce_get_tuning(B.FLCE_TUNE_SM_PAIRS) == pair
+        assert B.flce_get_tuning(B.FLCE_TUNE_WIDE_TILES) == wide
+        label = f"pair={pair} wide={wide}"
         assert_full_parity(make_inputs("ragged", dtype="bf16"), "mean", grad_loss=1.25,
-                           label=f"ragged-bf16 pair={pair}")
+                           label=f"ragged-bf16 {label}")
         assert_full_parity(make_inputs("tiny", T=300, H=264, V=700, dtype="bf16", seed=21), "sum",
-                           label=f"300x264x700 pair={pair}")
+                           label=f"300x264x700 {label}")
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
+        B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
         B.flce_set_backward_slab_width(0)
+
+
+def test_contraction_cores_agree():
+    """The three contraction cores (single-SM, SM pairs with 128-row and with 256-row CTA tiles)
+    sum every output element over K in the same order, so all outputs agree bit for bit."""
+    inp = make_inputs("tiny", T=1100, H=320, V=3000, dtype="bf16", seed=33)
+    x, w, y = to_device(inp)
+    outs = []
+    try:
+        for pair, wide in [(0, 0), (7, 0), (7, 7)]:
+            B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
+            B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
+            loss, lse, status = A.flce_forward(x, w, y, "mean")
+            gx, gw, status_b = A.flce_backward(x, w, y, lse, torch.ones((), device="cuda"), "mean")
+            torch.cuda.synchronize()
+            A.check_status(status)
+            A.check_status(status_b)
+            outs.append([loss.cpu().numpy(), lse.cpu().numpy(), gx.float().cpu().numpy(),
+                         gw.float().cpu().numpy()])
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
+        B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert np.array_equal(a, b)
 
 
 @pytest.mark.parametrize("T,H,V,dtype", [
@@ -399,10 +431,12 @@ def test_parity_forward_backward_single_call(name, T, H, V, dtype, reduction):
     assert e_gx <= tol["grad"] and e_gw <= tol["grad"]
 
 
-@pytest.mark.parametrize("pair", [0, 4])
-def test_single_call_gradient_tiles_single_sm_and_sm_pairs(pair):
-    """The single call's dynamically scheduled gradient launch on single SMs and on SM pairs."""
+@pytest.mark.parametrize("pair,wide", [(0, 0), (4, 0), (4, 4), (5, 5)])
+def test_single_call_gradient_tiles_single_sm_and_sm_pairs(pair, wide):
+    """The single call's dynamically scheduled gradient launch on single SMs, on SM pairs with
+    128-row and with 256-row CTA tiles (and its chunk logits on wide pair tiles, mask 5)."""
     B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
+    B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
     try:
         for name, red in [("ragged", "mean"), ("llama2_head", "none")]:
             inp = make_inputs(name, dtype="bf16")
@@ -413,10 +447,12 @@ def test_single_call_gradient_tiles_single_sm_and_sm_pairs(pair):
             ref = oracle.flce(inp.x, inp.weight, inp.target, red, grad_loss=gl)
             e_gx = norm_err(gx, ref["grad_x"])
             e_gw = norm_err(gw, ref["grad_weight"])
-            print(f"single call pair={pair} {name}/{red}: gx {e_gx:.3e} gw {e_gw:.3e}")
+            print(f"single call pair={pair} wide={wide} {name}/{red}: gx {e_gx:.3e} "
+                  f"gw {e_gw:.3e}")
             assert e_gx <= TOL["bf16"]["grad"] and e_gw <= TOL["bf16"]["grad"]
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
+        B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
 
 
 def test_single_call_is_deterministic_and_agrees_with_two_calls():
