@@ -513,6 +513,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
                 "copy_ms_per_step": statistics.median(e2e_copy_ms),
                 "compute_ms_per_step": statistics.median(e2e_comp_ms),
                 "compute_ms_steps": [round(v, 3) for v in e2e_comp_ms],
+                "copy_ms_steps": [round(v, 3) for v in e2e_copy_ms],
                 "gap_ms_steps": [round(comp_ev[k][1].elapsed_time(comp_ev[k + 1][0]), 3)
                                  for k in range(e2e_steps - 1)],
                 "h2d_bytes_per_step": int(hx.numel() * hx.element_size() +

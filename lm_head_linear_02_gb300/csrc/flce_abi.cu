@@ -184,6 +184,7 @@ struct Carver {
 
 struct FwdWs {
   float *part_m, *part_s, *zy, *block_sums;
+  int* counter;                      // tile counter of the projection launch
   float *x_hi, *x_lo, *w_hi, *w_lo;  // f32 path only
 };
 
@@ -194,6 +195,7 @@ size_t carve_fwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, FwdWs* w
   r.part_s = static_cast<float*>(c.take(sizeof(float) * nt * T));
   r.zy = static_cast<float*>(c.take(sizeof(float) * T));
   r.block_sums = static_cast<float*>(c.take(sizeof(float) * cdiv(T, 256)));
+  r.counter = static_cast<int*>(c.take(sizeof(int)));
   if (dtype == FLCE_DTYPE_F32) {
     r.x_hi = static_cast<float*>(c.take(sizeof(float) * T * H));
     r.x_lo = static_cast<float*>(c.take(sizeof(float) * T * H));
@@ -226,6 +228,7 @@ struct BwdWs {
   float* acc;     // bf16 path, [T][H] when more than one slab
   float *x_hi, *x_lo, *xt_hi, *xt_lo;  // [T][H], [H][ldT]
   float *w_hi, *w_lo, *wt_hi, *wt_lo;  // [V][H], [H][ldV]
+  int* counter;                        // tile counter of the dz and gradient launches
 };
 
 size_t carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, BwdWs* w) {
@@ -251,6 +254,7 @@ size_t carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, BwdWs* w
     r.wt_hi = static_cast<float*>(c.take(sizeof(float) * H * r.ldV));
     r.wt_lo = static_cast<float*>(c.take(sizeof(float) * H * r.ldV));
   }
+  r.counter = static_cast<int*>(c.take(sizeof(int)));
   if (w) *w = r;
   return c.off;
 }
@@ -501,6 +505,7 @@ int flce_forward(const void* x, const void* weight, const int64_t* target, int64
   p.lse = lse;
   p.loss = loss;
   p.status = status;
+  p.tile_counter = w.counter;
   p.T = int(T);
   p.H = int(H);
   p.V = int(V);
@@ -622,6 +627,7 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
     dz.slab0 = int(slab0);
     dz.slab_w = int(sw);
     dz.status = status;
+    dz.tile_counter = w.counter;
     dz.sms = dev.sms;
     dz.stream = s;
 
@@ -634,6 +640,7 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
     gw.slab0 = int(slab0);
     gw.slab_w = int(sw);
     gw.status = status;
+    gw.tile_counter = w.counter;
     gw.sms = dev.sms;
     gw.stream = s;
 

@@ -30,6 +30,7 @@ cudaError_t launch_dz_bf16(const CUtensorMap& tx, const CUtensorMap& tw_slab, co
     g.p[0] = make_problem(p.T, p.slab_w, p.H, 64, false, false, core_tile_rows(core), 0);
     g.num_problems = 1;
     g.status = p.status;
+    g.tile_counter = p.tile_counter;
     return launch_pair_core<DzEpi<false>, NoEpi>(core, tx, tw_slab, tx, tw_slab, g, ea,
                                                  NoEpi::Args{}, p.sms, p.stream);
   }
@@ -73,6 +74,7 @@ cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
   g.p[1] = make_problem(px.T, px.H, px.K, 64, false, true, rows, g.p[0].m_tiles * g.p[0].n_tiles);
   g.num_problems = 2;
   g.status = pw.status;
+  g.tile_counter = pw.tile_counter;
   if (core != kCoreSingle)
     return launch_pair_core<GradWEpi<false>, GradXEpi<false>>(core, tdz_mn, tx_mn, tdz_k, tw_mn, g,
                                                               ew, ex, pw.sms, pw.stream);

@@ -62,6 +62,7 @@ cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
   g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, core_tile_rows(core), 0);
   g.num_problems = 1;
   g.status = c.status;
+  g.tile_counter = c.tile_counter;  // tiles in list order: the pairs sharing a W tile stay in step
   if (core != kCoreSingle)
     return launch_pair_core<LogitsEpi, NoEpi>(core, tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{}, c.sms,
                                               c.stream);

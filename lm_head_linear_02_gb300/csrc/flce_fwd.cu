@@ -86,6 +86,7 @@ static cudaError_t launch_forward(const CUtensorMap& tx, const CUtensorMap& tw,
   g.p[0] = make_problem(p.T, p.V, p.H, StageGeom<kTF32>::kBK, false, false, kBM, 0);
   g.num_problems = 1;
   g.status = p.status;
+  g.tile_counter = p.tile_counter;
   FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V};
   cudaError_t e = launch_gemm<kTF32, FwdEpi, NoEpi>(tx, tw, tx_lo, tw_lo, g, ea, NoEpi::Args{},
                                                     p.sms, p.stream);
@@ -128,6 +129,7 @@ cudaError_t launch_forward_bf16(const CUtensorMap& tx, const CUtensorMap& tw, co
     g.p[0] = make_problem(p.T, p.V, p.H, 64, false, false, core_tile_rows(core), 0);
     g.num_problems = 1;
     g.status = p.status;
+    g.tile_counter = p.tile_counter;
     FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V};
     cudaError_t e = launch_pair_core<FwdEpi, NoEpi>(core, tx, tw, tx, tw, g, ea, NoEpi::Args{},
                                                     p.sms, p.stream);

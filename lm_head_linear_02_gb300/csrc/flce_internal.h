@@ -79,6 +79,7 @@ struct FwdLaunch {
   float* block_sums;  // [ceil(T / 256)]
   float* lse;         // [T]
   float* loss;        // [1], or [T] for the 'none' reduction
+  int* tile_counter;  // zeroed before the projection launch: tiles handed out in list order
   int* status;
   int T, H, V, reduction;
   int sms;
@@ -111,6 +112,7 @@ struct DzLaunch {
   void* dzt_lo;       // fp32 [Vc][ldt] transposed lo (tf32 path)
   int ldz, ldt;
   int T, H, slab0, slab_w;
+  int* tile_counter;  // or null (static schedule)
   int* status;
   int sms;
   cudaStream_t stream;
@@ -124,6 +126,7 @@ struct GradWLaunch {
   const float* grad_loss;  // null for the 'none' reduction (g = scale = 1)
   float scale;   // 1 (sum, none) or 1/T (mean); g = grad_loss[0] * scale
   int H, T, slab0, slab_w;
+  int* tile_counter;  // or null (static schedule); the bf16 launch of both gradients uses it
   int* status;
   int sms;
   cudaStream_t stream;
@@ -146,7 +149,7 @@ struct GradXLaunch {
 };
 // bf16, one launch on CTA pairs (256 x 256 tiles) for both gradients of a slab:
 //   grad_W: A = dz slab (MN-major boxes {64 x 64}), B = x (MN-major boxes {64 x 64});
-//   grad_x: A = dz slab (K-major {64 x 128}), B = W slab (MN-major {64 x 64}).
+//   grad_x: A = dz slab (K-major {64 x core_a_box_rows}), B = W slab (MN-major {64 x 64}).
 cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
                               const CUtensorMap& tdz_k, const CUtensorMap& tw_mn,
                               const GradWLaunch& pw, const GradXLaunch& px);
