@@ -94,7 +94,7 @@ size_t flce_backward_workspace_size(int64_t T, int64_t H, int64_t V, int dtype);
 int64_t flce_backward_slab_width(int64_t T, int64_t H, int64_t V, int dtype);
 
 /* Process-wide override of the backward vocab slab width: vc = 0 restores the automatic choice
- * (a dz slab of at most 512 MiB), otherwise vc must be a positive multiple of 256. Affects the
+ * (a dz slab of at most 1 GiB), otherwise vc must be a positive multiple of 256. Affects the
  * size query and the backward alike, so set it before querying the workspace size. A tuning and
  * testing knob: it trades workspace memory against the number of slab passes. Returns FLCE_OK
  * or FLCE_ERR_ARG. */
@@ -136,7 +136,7 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
  * fused_linear_cross_entropy kernel" (Helion PR #1268) computes the gradients inside the forward
  * over token chunks; "feat(FLCE): add helion version of fused linear cross entropy"
  * (Liger-Kernel PR #928) calls its chunk-materialised backward "works fine". Here the logits of a
- * chunk of tokens (at most half of all tokens and at most 1 GiB of bf16) are computed once and
+ * chunk of tokens (at most half of all tokens and at most 2 GiB of bf16) are computed once and
  * turned into dz in place, so the call does 6 T H V FLOPs instead of the 8 T H V of
  * flce_forward + flce_backward, at the price of the chunk buffer and an fp32 grad_weight
  * accumulator in the workspace.

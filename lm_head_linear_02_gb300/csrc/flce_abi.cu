@@ -155,7 +155,10 @@ using flce::kTileN;
 constexpr int64_t kMaxDim = int64_t(1) << 24;          // T, V bound (tile counts fit in int)
 constexpr int64_t kMaxHidden = int64_t(1) << 20;
 constexpr size_t kAlign = 256;
-constexpr int64_t kSlabBudgetBytes = int64_t(512) << 20;  // dz slab (all its copies) per slab
+// dz slab (all its copies) per slab. Each slab costs one read-modify-write pass over the fp32
+// grad_x accumulator; 1 GiB (4 slabs at T = 16384, V = 128256) measured 1.5% faster per step
+// than 512 MiB (8 slabs).
+constexpr int64_t kSlabBudgetBytes = int64_t(1) << 30;
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
@@ -271,7 +274,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // ---- single-call forward + backward (token chunks, no logits recompute)
 
-constexpr int64_t kChunkBudgetBytes = int64_t(1) << 30;  // bf16 chunk logits per chunk
+// bf16 chunk logits per chunk. Larger chunks mean fewer fp32 read-modify-write passes over the
+// grad_weight accumulator (one per chunk): 2 GiB halves them against 1 GiB at V = 128256
+// (measured: the single call's gradient launches 20.3 -> 18.5 ms per step at T = 16384).
+constexpr int64_t kChunkBudgetBytes = int64_t(1) << 31;
 constexpr int64_t kMinFusedTokens = 512;
 
 // The chunked single-call schedule applies to bf16 with at least 512 tokens (so a chunk never

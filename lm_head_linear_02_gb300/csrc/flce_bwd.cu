@@ -59,8 +59,8 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
 // grad_W (A = dz slab, B = x, both MN-major, K = T) and grad_x (A = dz slab K-major, B = W slab
 // MN-major, K = slab width) of one slab in a single launch: both read only the dz slab written
 // by the preceding dz launch, and one combined tile list fills the GPU evenly (two separate
-// launches of 2048 tiles each would leave the last of their 13.5 waves half empty).
-// Single-CTA 128 x 256 tiles, or 256 x 256 tiles on CTA pairs (FLCE_ROLE_GRADS in the pair mask).
+// launches would each end in a partly filled last wave). The problem with the longer K (the
+// longer tiles) is listed first, so that the tiles handed out last are the short ones.
 cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
                               const CUtensorMap& tdz_k, const CUtensorMap& tw_mn,
                               const GradWLaunch& pw, const GradXLaunch& px) {
@@ -69,12 +69,25 @@ cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
                                     px.T,     px.H,      px.mode};
   const Core core = role_core(pw.sms, FLCE_ROLE_GRADS);  // dz K-major map boxed to match
   const int rows = core_tile_rows(core);
+  const GemmProblem w = make_problem(pw.slab_w, pw.H, pw.T, 64, true, true, rows, 0);
+  const GemmProblem x = make_problem(px.T, px.H, px.K, 64, false, true, rows, 0);
   GemmGrid g{};
-  g.p[0] = make_problem(pw.slab_w, pw.H, pw.T, 64, true, true, rows, 0);
-  g.p[1] = make_problem(px.T, px.H, px.K, 64, false, true, rows, g.p[0].m_tiles * g.p[0].n_tiles);
   g.num_problems = 2;
   g.status = pw.status;
   g.tile_counter = pw.tile_counter;
+  if (x.k_blocks > w.k_blocks) {  // grad_x tiles first
+    g.p[0] = x;
+    g.p[1] = w;
+    g.p[1].tile_begin = x.m_tiles * x.n_tiles;
+    if (core != kCoreSingle)
+      return launch_pair_core<GradXEpi<false>, GradWEpi<false>>(core, tdz_k, tw_mn, tdz_mn, tx_mn,
+                                                                g, ex, ew, pw.sms, pw.stream);
+    return launch_gemm<false, GradXEpi<false>, GradWEpi<false>>(tdz_k, tw_mn, tdz_mn, tx_mn, g, ex,
+                                                                ew, pw.sms, pw.stream);
+  }
+  g.p[0] = w;
+  g.p[1] = x;
+  g.p[1].tile_begin = w.m_tiles * w.n_tiles;
   if (core != kCoreSingle)
     return launch_pair_core<GradWEpi<false>, GradXEpi<false>>(core, tdz_mn, tx_mn, tdz_k, tw_mn, g,
                                                               ew, ex, pw.sms, pw.stream);

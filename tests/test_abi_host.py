@@ -56,6 +56,7 @@ def test_workspace_sizes():
     bwd = B.flce_backward_workspace_size(T, H, V, B.FLCE_DTYPE_BF16)
     vc = B.flce_backward_slab_width(T, H, V, B.FLCE_DTYPE_BF16)
     assert vc % 256 == 0 and 256 <= vc <= V + 255
+    assert vc == 32768 and 2 * T * vc <= 1 << 30  # the largest slab of at most 1 GiB: 4 slabs
     assert bwd >= 2 * T * vc
     # never anything close to the tokens x vocab logits
     assert fwd + bwd < 2 * T * V
@@ -177,3 +178,21 @@ def test_tuning_knobs_validate(lib):
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
     assert B.flce_get_tuning(B.FLCE_TUNE_WIDE_TILES) == 7
+
+
+def test_single_call_chunk_rule(lib):
+    """Tokens per chunk of the single-call schedule: a multiple of 256, at most half of T (so no
+    chunk ever holds all tokens' logits) and at most 2 GiB of bf16 logits; bf16 only, T >= 512."""
+    bf16 = B.FLCE_DTYPE_BF16
+    assert B.flce_forward_backward_chunk_tokens(16384, 4096, 128256, bf16) == 8192
+    assert B.flce_forward_backward_chunk_tokens(32768, 4096, 128256, bf16) == 8192
+    assert B.flce_forward_backward_chunk_tokens(4096, 4096, 32000, bf16) == 2048
+    assert B.flce_forward_backward_chunk_tokens(1269, 1000, 10000, bf16) == 768
+    assert B.flce_forward_backward_chunk_tokens(300, 256, 1500, bf16) == 300  # below 512: T
+    assert B.flce_forward_backward_chunk_tokens(16384, 4096, 128256, B.FLCE_DTYPE_F32) == 16384
+    for T, V in [(16384, 128256), (32768, 151936), (8192, 262208), (600, 513), (100000, 50000)]:
+        c = B.flce_forward_backward_chunk_tokens(T, 4096, V, bf16)
+        ldz = -(-V // 256) * 256
+        assert c % 256 == 0 and c >= 256
+        assert c <= -(-T // 2 // 256) * 256 + 256 and c < T
+        assert c == 256 or 2 * c * ldz <= 1 << 31
