@@ -1,4 +1,5 @@
-// epilogues.cuh - what each FLCE kernel does with a finished 128 x 256 fp32 accumulator tile.
+// epilogues.cuh - what each FLCE kernel does with a finished 128 x 256 block of fp32
+// accumulators (one tile on the single-SM core; one CTA's share, or one half of it, on pairs).
 //
 // Every epilogue thread owns one accumulator row (one TMEM lane) and walks its 256 columns in
 // eight 32-column chunks (tcgen05.ld 32x32b.x32), so the per-row reductions of the softmax are

@@ -147,7 +147,7 @@ struct GradXLaunch {
   int sms;
   cudaStream_t stream;
 };
-// bf16, one launch on CTA pairs (256 x 256 tiles) for both gradients of a slab:
+// bf16, one launch (on the role's core) for both gradients of a slab, longer-K problem first:
 //   grad_W: A = dz slab (MN-major boxes {64 x 64}), B = x (MN-major boxes {64 x 64});
 //   grad_x: A = dz slab (K-major {64 x core_a_box_rows}), B = W slab (MN-major {64 x 64}).
 cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_mn,
