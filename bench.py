@@ -82,12 +82,42 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def sources_digest() -> str:
+def strip_comments(src: str) -> str:
+    """C/C++ source without comments and whitespace (string and character literals kept), so
+    that the digest below changes with the code only."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            i = src.find("*/", i + 2)
+            i = n if i < 0 else i + 2
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
+def sources_digest(read=None) -> str:
+    """SHA-256 over the comment-free kernel sources (the key of the recorded DRAM traffic)."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(CSRC, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    names = sorted(n for n in os.listdir(CSRC) if n.endswith((".cu", ".cuh", ".h")))
+    for name in names:
+        if read is None:
+            with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+                text = f.read()
+        else:
+            text = read(name)
+        h.update(name.encode() + b"\0" + strip_comments(text).encode())
     return h.hexdigest()
 
 
