@@ -220,11 +220,12 @@ int flce_set_tuning(int key, int64_t value);
  * Returns FLCE_OK, FLCE_ERR_ARG or FLCE_ERR_CUDA. */
 int flce_get_tuning(int key, int64_t* value);
 
-/* Testing aid for the failure path; never needed in normal use. The next single-SM contraction
- * launch withholds, in its first CTA only, the signal that its first accumulator tile is ready:
- * that CTA's epilogue wait then runs out of time (about 2 s) and the launch ends early with
- * FLCE_STATUS_TIMEOUT OR-ed into the status word and undefined outputs, instead of hanging.
- * One-shot: later launches are unaffected and the device stays usable. Returns FLCE_OK. */
+/* Testing aid for the failure path; never needed in normal use. The next bf16 or fp32
+ * contraction launch withholds, in its first CTA (or first CTA pair) only, the signal that its
+ * first accumulator tile is ready: that CTA's (that pair's) epilogue wait then runs out of time
+ * (about 2 s) and the launch ends early with FLCE_STATUS_TIMEOUT OR-ed into the status word and
+ * undefined outputs, instead of hanging. One-shot: later launches are unaffected and the device
+ * stays usable. Returns FLCE_OK. */
 int flce_test_withhold_signal(void);
 
 /* Static, human-readable name of a return code. Never NULL. */

@@ -46,7 +46,7 @@ struct GemmGrid {
   int* status;        // device status word (FLCE_STATUS_* bits)
   int* tile_counter;  // null: CTA b takes tiles b, b + grid, ...; else a zeroed device int that
                       // hands out tiles in list order to whichever CTA is free (dynamic)
-  int withhold;       // testing aid: CTA 0 does not signal its first accumulator tile
+  int withhold;       // testing aid: CTA 0 (pair 0) does not signal its first accumulator tile
 };
 
 // Depth of the per-CTA queue through which the producer hands tile indices to the MMA thread

@@ -267,7 +267,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
           }
         }
         if (!ok) break;
-        mma_commit_pair(tfull_bar(acc), 0x3);
+        // (g.withhold: the failure-path test leaves the first pair's first tile unsignalled so
+        // that both CTAs' epilogue waits run out.)
+        if (!(g.withhold && cluster_id == 0 && consumed == k_blocks))
+          mma_commit_pair(tfull_bar(acc), 0x3);
         if (++acc == G::kAccBufs) {
           acc = 0;
           acc_phase ^= 1u;
@@ -394,6 +397,7 @@ cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& b0, const CUte
     e = cudaMemsetAsync(g.tile_counter, 0, sizeof(int), stream);
     if (e != cudaSuccess) return e;
   }
+  g.withhold = take_withhold_request() ? 1 : 0;
   const int clusters = g.num_tiles < max_clusters ? g.num_tiles : max_clusters;
   kern<<<2 * clusters, G::kThreads, G::kSmemBytes, stream>>>(a0, b0, a1, b1, g, e0, e1);
   return cudaGetLastError();

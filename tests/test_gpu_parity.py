@@ -220,14 +220,18 @@ def test_out_of_range_target_sets_status_and_nan_loss():
         A.check_status(status)
 
 
-def test_pipeline_timeout_is_reported_and_device_stays_usable():
+@pytest.mark.parametrize("pair,wide", [(0, 0), (7, 0), (7, 7)])
+def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide):
     """A withheld pipeline signal ends the launch with FLCE_STATUS_TIMEOUT after the bounded wait
-    (about 2 s) instead of hanging; the next calls run normally on the same context."""
+    (about 2 s) instead of hanging, on each contraction core (single SM, SM pairs with 128-row
+    and with 256-row CTA tiles, whose abort path also drains the partner CTA); the next calls
+    run normally on the same context."""
     import time
 
     inp = make_inputs("ragged", dtype="bf16")
     x, w, y = to_device(inp)
-    B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, 0)  # the forward runs on the single-SM core
+    B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
+    B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
     try:
         B.flce_test_withhold_signal()
         t0 = time.time()
@@ -240,7 +244,8 @@ def test_pipeline_timeout_is_reported_and_device_stays_usable():
             A.check_status(status)
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
-    assert_full_parity(inp, "mean", label="after timeout")
+        B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
+    assert_full_parity(inp, "mean", label=f"after timeout pair={pair} wide={wide}")
 
 
 def test_sum_mean_and_grad_loss_scaling():
