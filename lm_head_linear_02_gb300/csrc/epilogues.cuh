@@ -233,18 +233,32 @@ struct DzEpi {
     const float rs = (valid && a.row_scale) ? __ldg(a.row_scale + t) : 1.0f;
     const int n0 = nb * kBN;  // slab-relative column of the tile
     const long long rel = y - a.slab0 - n0;
+    const bool unit_scale = a.row_scale == nullptr;  // uniform: sum / mean reductions
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
       const int c0 = n0 + c * 32;
       if (c0 >= a.slab_w) break;  // uniform
       float v[32];
       load_chunk(taddr, c, v);
+      if (unit_scale && c0 + 32 <= a.slab_w) {
+        // The common case: every column inside the slab and row factor 1, so only the one
+        // target column of a row (if it lies in this chunk) differs from exp(z - lse).
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float d = ex2(fmaf(v[j], kLog2e, -lsel));
-        if (rel == c * 32 + j) d -= 1.0f;
-        if (c0 + j >= a.slab_w) d = 0.f;
-        v[j] = d * rs;
+        for (int j = 0; j < 32; ++j) v[j] = ex2(fmaf(v[j], kLog2e, -lsel));
+        const long long q = rel - c * 32;
+        if (q >= 0 && q < 32) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == q) v[j] -= 1.0f;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float d = ex2(fmaf(v[j], kLog2e, -lsel));
+          if (rel == c * 32 + j) d -= 1.0f;
+          if (c0 + j >= a.slab_w) d = 0.f;
+          v[j] = d * rs;
+        }
       }
       if (!valid) continue;
       if constexpr (!kTF32) {

@@ -3,6 +3,8 @@
 //   grad_W : grad_W[slab] = dz_slab^T . x                                     (K = T, complete)
 //   grad_x : grad_x (+)= dz_slab . W_slab                                     (split-K over slabs)
 // plus the TF32 hi/lo operand split used by the fp32 path.
+#include <atomic>
+
 #include "epilogues.cuh"
 #include "flce_internal.h"
 #include "gemm_pair.cuh"
@@ -98,13 +100,27 @@ cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
 int pair_roles(int sms) {
   const int t = tune_sm_pairs();
   if (t >= 0) return t;
-  auto kern = k_umma_gemm_pair<128, GradWEpi<false>, GradXEpi<false>>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           PairGeom<128>::kSmemBytes) != cudaSuccess) {
+  // Automatic choice, decided once per device: all roles on pairs when every SM can hold half
+  // of a resident pair of the kernel the automatic choice launches (wide tiles).
+  static std::atomic<int> decided[64];  // 0: not yet; else mask + 1
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  return 2 * pair_resident_clusters<128>(kern, sms) >= 2 * (sms / 2) ? kAutoPairRoles : 0;
+  if (dev >= 0 && dev < 64) {
+    const int d = decided[dev].load();
+    if (d) return d - 1;
+  }
+  auto kern = k_umma_gemm_pair<256, GradXEpi<false>, GradWEpi<false>>;
+  int mask = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           PairGeom<256>::kSmemBytes) == cudaSuccess)
+    mask = 2 * pair_resident_clusters<256>(kern, sms) >= 2 * (sms / 2) ? kAutoPairRoles : 0;
+  else
+    cudaGetLastError();
+  if (dev >= 0 && dev < 64) decided[dev].store(mask + 1);
+  return mask;
 }
 
 cudaError_t launch_gradw_tf32(const CUtensorMap& tdzt_hi, const CUtensorMap& txt_hi,
