@@ -219,7 +219,9 @@ int64_t slab_width(int64_t T, int64_t V, int dtype) {
   const int64_t per_col = dtype == FLCE_DTYPE_BF16 ? 2 * T : 16 * round_up(T, 4);
   int64_t vc = kSlabBudgetBytes / per_col / kTileN * kTileN;
   if (vc < kTileN) vc = kTileN;
-  return vc < vmax ? vc : vmax;
+  if (vc >= vmax) return vmax;
+  // As few slabs as the budget allows, of (nearly) equal width: no narrow last slab.
+  return round_up(cdiv(V, cdiv(V, vc)), kTileN);
 }
 
 struct BwdWs {
@@ -291,7 +293,9 @@ int64_t fused_chunk_rows(int64_t T, int64_t V) {
   int64_t c = kChunkBudgetBytes / (2 * ldz) / 256 * 256;
   const int64_t half = round_up(cdiv(T, 2), 256);
   if (c > half) c = half;
-  return c < 256 ? 256 : c;
+  if (c < 256) c = 256;
+  // As few chunks as the limits allow, of (nearly) equal size: no small last chunk.
+  return round_up(cdiv(T, cdiv(T, c)), 256);
 }
 
 struct FusedWs {

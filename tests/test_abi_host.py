@@ -56,7 +56,10 @@ def test_workspace_sizes():
     bwd = B.flce_backward_workspace_size(T, H, V, B.FLCE_DTYPE_BF16)
     vc = B.flce_backward_slab_width(T, H, V, B.FLCE_DTYPE_BF16)
     assert vc % 256 == 0 and 256 <= vc <= V + 255
-    assert vc == 32768 and 2 * T * vc <= 1 << 30  # the largest slab of at most 1 GiB: 4 slabs
+    # as few slabs of at most 1 GiB as possible (4), of nearly equal width
+    assert vc == 32256 and 2 * T * vc <= 1 << 30 and -(-V // vc) == 4
+    # Gemma-3-sized head: 5 balanced slabs, not 4 wide ones and a 64-column sliver
+    assert B.flce_backward_slab_width(8192, 2304, 262208, B.FLCE_DTYPE_BF16) == 52480
     assert bwd >= 2 * T * vc
     # never anything close to the tokens x vocab logits
     assert fwd + bwd < 2 * T * V
@@ -190,6 +193,8 @@ def test_single_call_chunk_rule(lib):
     assert B.flce_forward_backward_chunk_tokens(1269, 1000, 10000, bf16) == 768
     assert B.flce_forward_backward_chunk_tokens(300, 256, 1500, bf16) == 300  # below 512: T
     assert B.flce_forward_backward_chunk_tokens(16384, 4096, 128256, B.FLCE_DTYPE_F32) == 16384
+    # Gemma-3-sized head: 3 chunks of nearly equal size (2816 + 2816 + 2560), not 3840 + 3840 + 512
+    assert B.flce_forward_backward_chunk_tokens(8192, 2304, 262208, bf16) == 2816
     for T, V in [(16384, 128256), (32768, 151936), (8192, 262208), (600, 513), (100000, 50000)]:
         c = B.flce_forward_backward_chunk_tokens(T, 4096, V, bf16)
         ldz = -(-V // 256) * 256
