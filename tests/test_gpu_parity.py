@@ -159,10 +159,11 @@ def test_parity_single_sm_and_sm_pair_tiles(pair, wide):
 
 def test_contraction_cores_agree():
     """The three contraction cores (single-SM, SM pairs with 128-row and with 256-row CTA tiles)
-    sum every output element over K in the same order, so all outputs agree bit for bit."""
+    sum every output element over K in the same order, so all outputs agree bit for bit, for
+    both schedules."""
     inp = make_inputs("tiny", T=1100, H=320, V=3000, dtype="bf16", seed=33)
     x, w, y = to_device(inp)
-    outs = []
+    outs, fused = [], []
     try:
         for pair, wide in [(0, 0), (7, 0), (7, 7)]:
             B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
@@ -174,11 +175,16 @@ def test_contraction_cores_agree():
             A.check_status(status_b)
             outs.append([loss.cpu().numpy(), lse.cpu().numpy(), gx.float().cpu().numpy(),
                          gw.float().cpu().numpy()])
+            fused.append(run_fused(x, w, y, "mean", 1.0))
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
     for other in outs[1:]:
         for a, b in zip(outs[0], other):
+            assert np.array_equal(a, b)
+    for other in fused[1:]:  # the single call (chunks of 768 and 332 tokens) on each core
+        assert fused[0][0] == other[0]
+        for a, b in zip(fused[0][1:], other[1:]):
             assert np.array_equal(a, b)
 
 
@@ -383,11 +389,15 @@ def test_large_batch_memory_and_sampled():
 
 @pytest.mark.parametrize("name", ["qwen3_head_t32768", "gemma3_head_t8192"])
 def test_second_workloads_sampled(name):
-    """The Qwen3 and Gemma3 heads of the Liger-Kernel benchmarks at full size."""
+    """The Qwen3 and Gemma3 heads of the Liger-Kernel benchmarks at full size, both schedules
+    (the single call splits the tokens into chunks of nearly equal size: 5 x 6656 and 3 x 2816)."""
     inp = make_inputs(name)
-    T = inp.workload.T
-    rows = np.unique(np.concatenate([[0, T - 1], np.random.default_rng(T + 1).integers(0, T, 14)]))
+    T, H, V = inp.workload.T, inp.workload.H, inp.workload.V
+    chunk = B.flce_forward_backward_chunk_tokens(T, H, V, B.FLCE_DTYPE_BF16)
+    edges = [0, chunk - 1, chunk, T - 1]
+    rows = np.unique(np.concatenate([edges, np.random.default_rng(T + 1).integers(0, T, 12)]))
     _sampled_checks(inp, rows, name)
+    _sampled_checks(inp, rows, name + " single call", fused=True)
 
 
 # ------------------------------------------------------------------ single-call forward + backward
@@ -477,8 +487,10 @@ def test_single_call_is_deterministic_and_agrees_with_two_calls():
 
 def test_single_call_full_size_headline():
     inp = make_inputs("llama3_head_t16384")
-    T = inp.workload.T
-    rows = np.unique(np.concatenate([[0, 4095, 4096, T - 1], np.random.default_rng(3).integers(0, T, 12)]))
+    T, H, V = inp.workload.T, inp.workload.H, inp.workload.V
+    chunk = B.flce_forward_backward_chunk_tokens(T, H, V, B.FLCE_DTYPE_BF16)  # 8192
+    edges = [0, chunk - 1, chunk, T - 1]
+    rows = np.unique(np.concatenate([edges, np.random.default_rng(3).integers(0, T, 12)]))
     _sampled_checks(inp, rows, "single call llama3_head_t16384", fused=True)
 
 
