@@ -49,6 +49,32 @@ __device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32], i
     if (q * 4 < n) d[q] = make_float4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
 }
 
+// Store 32 rows x 32 bf16 columns held one row per lane (value j of lane r at row row0 + r,
+// column j of `base`), as 16-byte stores of 8 rows x 64 bytes each instead of 32 scattered
+// 16-byte pieces: the block passes through the warp's 2 KB of shared memory, its 16-byte units
+// XOR-swizzled by row so that the writes and the transposed reads are both free of bank
+// conflicts. Rows at or beyond `nrows` are not stored. Every lane of the warp must call this.
+__device__ __forceinline__ void store_rows_bf16x32(uint4* stage, const float (&v)[32], int lane,
+                                                   __nv_bfloat16* base, size_t ld, int row0,
+                                                   int nrows) {
+  const int sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    stage[lane * 4 + (k ^ sw)] =
+        make_uint4(pack_bf16x2(v[8 * k + 0], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                   pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+  __syncwarp();
+  const int a = lane >> 2, b = lane & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int r = 8 * q + a;
+    const uint4 w = stage[r * 4 + (b ^ ((r >> 1) & 3))];
+    if (row0 + r < nrows)
+      *reinterpret_cast<uint4*>(base + static_cast<size_t>(row0 + r) * ld + b * 8) = w;
+  }
+  __syncwarp();  // the next block may overwrite the staging area
+}
+
 // TF32 split of an fp32 value: hi keeps the top 10 mantissa bits (rounded to nearest), and
 // lo = x - hi is exact in fp32. hi + lo == x.
 __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
@@ -76,7 +102,7 @@ struct FwdEpi {
   static __device__ __forceinline__ void init(const Args&, State&) {}
 
   static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
-                                              uint32_t taddr) {
+                                              uint32_t taddr, uint4* stage) {
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
     const int n0 = nb * kBN;
@@ -150,7 +176,7 @@ struct LogitsEpi {
   static __device__ __forceinline__ void init(const Args&, State&) {}
 
   static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
-                                              uint32_t taddr) {
+                                              uint32_t taddr, uint4* stage) {
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
     const int n0 = nb * kBN;
@@ -187,8 +213,7 @@ struct LogitsEpi {
         v[j] -= m;
         v[j + 1] -= m;
       }
-      if (valid)
-        store_bf16x32(a.zbuf + static_cast<size_t>(t) * a.ldz + c0, v, 32);
+      store_rows_bf16x32(stage, v, row & 31, a.zbuf + c0, a.ldz, t - (row & 31), a.T);
     }
     if (valid) {
       const size_t o = static_cast<size_t>(nb) * a.T + t;
@@ -225,7 +250,7 @@ struct DzEpi {
   static __device__ __forceinline__ void init(const Args&, State&) {}
 
   static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
-                                              uint32_t taddr) {
+                                              uint32_t taddr, uint4* stage) {
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
     const float lsel = valid ? __ldg(a.lse + t) * kLog2e : 0.f;
@@ -260,11 +285,11 @@ struct DzEpi {
           v[j] = d * rs;
         }
       }
-      if (!valid) continue;
       if constexpr (!kTF32) {
-        store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.dz) + static_cast<size_t>(t) * a.ldz + c0,
-                      v, 32);
+        store_rows_bf16x32(stage, v, row & 31, reinterpret_cast<__nv_bfloat16*>(a.dz) + c0,
+                           static_cast<size_t>(a.ldz), t - (row & 31), a.T);
       } else {
+        if (!valid) continue;
         float hi[32], lo[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) split_tf32(v[j], hi[j], lo[j]);
@@ -306,7 +331,7 @@ struct GradWEpi {
   }
 
   static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
-                                              uint32_t taddr) {
+                                              uint32_t taddr, uint4*) {
     const int r = mb * kBM + row;  // slab-relative vocab row
     const bool valid = r < a.slab_w;
     const size_t vrow = static_cast<size_t>(a.slab0) + r;
@@ -354,7 +379,7 @@ struct GradXEpi {
   }
 
   static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
-                                              uint32_t taddr) {
+                                              uint32_t taddr, uint4*) {
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
 #pragma unroll 1

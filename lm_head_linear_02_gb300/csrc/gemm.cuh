@@ -25,6 +25,8 @@ namespace flce {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kThreads = 192;
+// Shared memory each epilogue warp owns for transposing its stores (32 rows x 64 bytes).
+constexpr uint32_t kEpiStageBytes = 2048;
 constexpr int kEpiWarp0 = 2;
 constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
 
@@ -91,14 +93,16 @@ struct StageGeom {
   static constexpr int kStages = kTF32x3 ? 2 : 4;
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
   // ring + barriers/bookkeeping + 1 KB alignment slack
-  static constexpr uint32_t kSmemBytes = kRingBytes + 1024 + 1024;
+  // ring, barrier/slot block (1 KB), 2 KB of store staging per epilogue warp, alignment slack
+  static constexpr uint32_t kSmemBytes = kRingBytes + 1024 + 4 * kEpiStageBytes + 1024;
 };
 
 struct NoEpi {
   struct Args {};
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
-  static __device__ __forceinline__ void tile(const Args&, State&, int, int, int, uint32_t) {}
+  static __device__ __forceinline__ void tile(const Args&, State&, int, int, int, uint32_t,
+                                              uint4*) {}
 };
 
 // A stage holds [A_hi][A_lo][B_hi][B_lo] (lo copies only for kTF32x3, whose operands are
@@ -318,6 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ epilogue
     const int quarter = warp & 3;  // TMEM lane group this warp may access
     const int row = quarter * 32 + lane;
+    uint4* stage = reinterpret_cast<uint4*>(smem + G::kRingBytes + 1024 +
+                                            static_cast<uint32_t>(warp - 2) * kEpiStageBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     typename Epi0::State st0;
@@ -343,9 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(quarter * 32) << 16);
       if (ti.prob == 0)
-        Epi0::tile(e0, st0, ti.mb, ti.nb, row, taddr);
+        Epi0::tile(e0, st0, ti.mb, ti.nb, row, taddr, stage);
       else
-        Epi1::tile(e1, st1, ti.mb, ti.nb, row, taddr);
+        Epi1::tile(e1, st1, ti.mb, ti.nb, row, taddr, stage);
       tc_fence_before_sync();
       mbar_arrive(tempty_bar(acc));
       if (++acc == 2) {

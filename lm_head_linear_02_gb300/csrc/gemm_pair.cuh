@@ -41,9 +41,10 @@ struct PairGeom {
   static constexpr uint32_t kBBytes = 128 * 128;       // this CTA's 128 N rows x 64 bf16
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
-  static constexpr uint32_t kSmemBytes = kRingBytes + 1024 + 1024;
   static constexpr int kAccBufs = 2 / kHalves;         // accumulators in the 512 TMEM columns
   static constexpr int kEpiWarps = 4 * kHalves;
+  // ring, barrier/slot block (1 KB), store staging per epilogue warp, alignment slack
+  static constexpr uint32_t kSmemBytes = kRingBytes + 1024 + kEpiWarps * kEpiStageBytes + 1024;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kTileRows = 2 * kRows;          // M rows of one pair tile
 };
@@ -284,6 +285,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
+    uint4* stage = reinterpret_cast<uint4*>(smem + kPairRingBytes + 1024 +
+                                            static_cast<uint32_t>(warp - 2) * kEpiStageBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     typename Epi0::State st0;
@@ -310,9 +313,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
       const uint32_t taddr = tmem_base + static_cast<uint32_t>((acc * G::kHalves + half) * kBN) +
                              (static_cast<uint32_t>(quarter * 32) << 16);
       if (pt.prob == 0)
-        Epi0::tile(e0, st0, mb128, pt.nb, row, taddr);
+        Epi0::tile(e0, st0, mb128, pt.nb, row, taddr, stage);
       else
-        Epi1::tile(e1, st1, mb128, pt.nb, row, taddr);
+        Epi1::tile(e1, st1, mb128, pt.nb, row, taddr, stage);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
