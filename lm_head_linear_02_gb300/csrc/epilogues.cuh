@@ -49,30 +49,44 @@ __device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32], i
     if (q * 4 < n) d[q] = make_float4(v[q * 4 + 0], v[q * 4 + 1], v[q * 4 + 2], v[q * 4 + 3]);
 }
 
-// Store 32 rows x 32 bf16 columns held one row per lane (value j of lane r at row row0 + r,
-// column j of `base`), as 16-byte stores of 8 rows x 64 bytes each instead of 32 scattered
-// 16-byte pieces: the block passes through the warp's 2 KB of shared memory, its 16-byte units
-// XOR-swizzled by row so that the writes and the transposed reads are both free of bank
-// conflicts. Rows at or beyond `nrows` are not stored. Every lane of the warp must call this.
-__device__ __forceinline__ void store_rows_bf16x32(uint4* stage, const float (&v)[32], int lane,
-                                                   __nv_bfloat16* base, size_t ld, int row0,
-                                                   int nrows) {
+// Exchange a warp's block of 32 rows x 64 bytes, held one row per lane (in[k] = bytes
+// [16k, 16k + 16) of lane r's row), so that lane 4a + b ends with out[q] = bytes [16b, 16b + 16)
+// of row 8q + a: afterwards each warp-wide 16-byte access covers 8 rows x 64 contiguous bytes
+// instead of 32 scattered 16-byte pieces. The block passes through the warp's 2 KB of shared
+// memory with its 16-byte units XOR-swizzled by row, so that the writes and the transposed
+// reads are both free of bank conflicts. Every lane of the warp must call this.
+__device__ __forceinline__ void transpose_rows64(uint4* stage, const uint4 (&in)[4],
+                                                 uint4 (&out)[4], int lane) {
   const int sw = (lane >> 1) & 3;
 #pragma unroll
-  for (int k = 0; k < 4; ++k)
-    stage[lane * 4 + (k ^ sw)] =
-        make_uint4(pack_bf16x2(v[8 * k + 0], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
-                   pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+  for (int k = 0; k < 4; ++k) stage[lane * 4 + (k ^ sw)] = in[k];
   __syncwarp();
   const int a = lane >> 2, b = lane & 3;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int r = 8 * q + a;
-    const uint4 w = stage[r * 4 + (b ^ ((r >> 1) & 3))];
-    if (row0 + r < nrows)
-      *reinterpret_cast<uint4*>(base + static_cast<size_t>(row0 + r) * ld + b * 8) = w;
+    out[q] = stage[r * 4 + (b ^ ((r >> 1) & 3))];
   }
   __syncwarp();  // the next block may overwrite the staging area
+}
+
+// Store 32 rows x 32 bf16 columns held one row per lane (value j of lane r at row row0 + r,
+// column j of `base`) through transpose_rows64. Rows at or beyond `nrows` are not stored.
+__device__ __forceinline__ void store_rows_bf16x32(uint4* stage, const float (&v)[32], int lane,
+                                                   __nv_bfloat16* base, size_t ld, int row0,
+                                                   int nrows) {
+  uint4 in[4], out[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    in[k] = make_uint4(pack_bf16x2(v[8 * k + 0], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                       pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+  transpose_rows64(stage, in, out, lane);
+  const int a = lane >> 2, b = lane & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int r = row0 + 8 * q + a;
+    if (r < nrows) *reinterpret_cast<uint4*>(base + static_cast<size_t>(r) * ld + b * 8) = out[q];
+  }
 }
 
 // TF32 split of an fp32 value: hi keeps the top 10 mantissa bits (rounded to nearest), and
@@ -331,24 +345,43 @@ struct GradWEpi {
   }
 
   static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
-                                              uint32_t taddr, uint4*) {
+                                              uint32_t taddr, uint4* stage) {
     const int r = mb * kBM + row;  // slab-relative vocab row
     const bool valid = r < a.slab_w;
     const size_t vrow = static_cast<size_t>(a.slab0) + r;
+    const int lane = row & 31;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
       const int h0 = nb * kBN + c * 32;
       if (h0 >= a.H) break;
       float v[32];
       load_chunk(taddr, c, v);
-      if (!valid) continue;
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= st.g;
-      const int n = min(32, a.H - h0);
-      if constexpr (kF32Out)
-        store_f32x32(reinterpret_cast<float*>(a.grad_w) + vrow * a.H + h0, v, n);
-      else
-        store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.grad_w) + vrow * a.H + h0, v, n);
+      if constexpr (kF32Out) {
+        if (valid) store_f32x32(reinterpret_cast<float*>(a.grad_w) + vrow * a.H + h0, v,
+                                min(32, a.H - h0));
+      } else {
+        // 8 bf16 columns per 16-byte unit; H is a multiple of 8, so units are whole or absent
+        uint4 in[4], out[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          in[k] = make_uint4(pack_bf16x2(v[8 * k + 0], v[8 * k + 1]),
+                             pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                             pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
+                             pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+        transpose_rows64(stage, in, out, lane);
+        const int qa = lane >> 2, qb = lane & 3;
+        const int r0 = r - lane;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int rr = r0 + 8 * q + qa;
+          const int col = h0 + qb * 8;
+          if (rr < a.slab_w && col < a.H)
+            *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.grad_w) +
+                                      (static_cast<size_t>(a.slab0) + rr) * a.H + col) = out[q];
+        }
+      }
     }
   }
 };
@@ -379,38 +412,102 @@ struct GradXEpi {
   }
 
   static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
-                                              uint32_t taddr, uint4*) {
+                                              uint32_t taddr, uint4* stage) {
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
+    if constexpr (!kF32Out) {
+      // Each 32-column chunk in two 16-column halves of fp32 (64 bytes per row), transposed
+      // through shared memory: lane 4a + b then owns columns [4b, 4b + 4) of rows 8q + a, and
+      // every accumulator read, accumulator write and output store is coalesced.
+      const int lane = row & 31;
+      const int qa = lane >> 2, qb = lane & 3;
+      const int t0 = t - lane;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      const int h0 = nb * kBN + c * 32;
-      if (h0 >= a.H) break;
-      float v[32];
-      load_chunk(taddr, c, v);
-      if (!valid) continue;
-      const int n = min(32, a.H - h0);
-      const size_t o = static_cast<size_t>(t) * a.H + h0;
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int h0 = nb * kBN + c * 32;
+        if (h0 >= a.H) break;
+        float v[32];
+        load_chunk(taddr, c, v);
+        // both 16-column halves through shared memory first, then every accumulator load of
+        // the chunk in flight at once, then the adds and stores
+        uint4 out[2][4];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= st.g;
-      if (a.mode >= 2) {
-        const float4* s = reinterpret_cast<const float4*>(a.acc + o);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint4 in[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (q * 4 < n) {
-            const float4 p = s[q];
-            v[q * 4 + 0] += p.x;
-            v[q * 4 + 1] += p.y;
-            v[q * 4 + 2] += p.z;
-            v[q * 4 + 3] += p.w;
+          for (int k = 0; k < 4; ++k)
+            in[k] = make_uint4(__float_as_uint(v[16 * hh + 4 * k + 0] * st.g),
+                               __float_as_uint(v[16 * hh + 4 * k + 1] * st.g),
+                               __float_as_uint(v[16 * hh + 4 * k + 2] * st.g),
+                               __float_as_uint(v[16 * hh + 4 * k + 3] * st.g));
+          transpose_rows64(stage, in, out[hh], lane);
+        }
+        float4 p[2][4];
+        if (a.mode >= 2) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int tr = t0 + 8 * q + qa;
+              const int col = h0 + 16 * hh + 4 * qb;  // H is a multiple of 8: 4-column units
+              p[hh][q] = (tr < a.T && col < a.H)
+                             ? *reinterpret_cast<const float4*>(a.acc + static_cast<size_t>(tr) * a.H + col)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int tr = t0 + 8 * q + qa;
+            const int col = h0 + 16 * hh + 4 * qb;
+            if (tr >= a.T || col >= a.H) continue;
+            const size_t o = static_cast<size_t>(tr) * a.H + col;
+            float4 d = make_float4(__uint_as_float(out[hh][q].x), __uint_as_float(out[hh][q].y),
+                                   __uint_as_float(out[hh][q].z), __uint_as_float(out[hh][q].w));
+            if (a.mode >= 2) {
+              d.x += p[hh][q].x;
+              d.y += p[hh][q].y;
+              d.z += p[hh][q].z;
+              d.w += p[hh][q].w;
+            }
+            if (a.mode == 1 || a.mode == 2) {
+              *reinterpret_cast<float4*>(a.acc + o) = d;
+            } else {
+              uint2 w;
+              w.x = pack_bf16x2(d.x, d.y);
+              w.y = pack_bf16x2(d.z, d.w);
+              *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + o) = w;
+            }
+          }
+      }
+    } else {  // fp32 outputs (the TF32 path): plain per-row stores
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int h0 = nb * kBN + c * 32;
+        if (h0 >= a.H) break;
+        float v[32];
+        load_chunk(taddr, c, v);
+        if (!valid) continue;
+        const int n = min(32, a.H - h0);
+        const size_t o = static_cast<size_t>(t) * a.H + h0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= st.g;
+        if (a.mode >= 2) {
+          const float4* s = reinterpret_cast<const float4*>(a.acc + o);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (q * 4 < n) {
+              const float4 p = s[q];
+              v[q * 4 + 0] += p.x;
+              v[q * 4 + 1] += p.y;
+              v[q * 4 + 2] += p.z;
+              v[q * 4 + 3] += p.w;
+            }
           }
         }
-      }
-      if (a.mode == 1 || a.mode == 2 || kF32Out) {
         store_f32x32((a.mode == 1 || a.mode == 2) ? a.acc + o : reinterpret_cast<float*>(a.out) + o,
                      v, n);
-      } else {
-        store_bf16x32(reinterpret_cast<__nv_bfloat16*>(a.out) + o, v, n);
       }
     }
   }
