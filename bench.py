@@ -519,6 +519,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
         torch.cuda.empty_cache()
         context = {"torch_eager": torch_eager_context(x, w, y)}
     pair_roles = B.flce_get_tuning(B.FLCE_TUNE_SM_PAIRS) if wl.dtype == "bf16" else 0
+    wide_roles = B.flce_get_tuning(B.FLCE_TUNE_WIDE_TILES) & pair_roles
     out = {
         "metric": METRIC, "value": whole_job_rate(T * args.steps, world, total_ms * 1e-3),
         "unit": UNIT,
@@ -527,7 +528,9 @@ def run_ours(args, wl, rank: int, world: int, dist):
         "data": "synthetic: seeded PCG64, x~N(0,1), weight~N(0,0.02^2), targets %s" % wl.target_dist,
         "config": dict(workload_config(wl, n_slabs),
                        sm_pair_roles=[n for n, b in (("forward", 1), ("dz", 2), ("grads", 4))
-                                      if pair_roles & b]),
+                                      if pair_roles & b],
+                       wide_tile_roles=[n for n, b in (("forward", 1), ("dz", 2), ("grads", 4))
+                                        if wide_roles & b]),
         "fwd_ms": statistics.median(fwd_ms), "bwd_ms": statistics.median(bwd_ms),
         "fwd_tokens_per_s": T / (statistics.median(fwd_ms) * 1e-3),
         "tensor_tflops_step": step_tflops,
