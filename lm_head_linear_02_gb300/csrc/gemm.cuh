@@ -1,4 +1,7 @@
-// gemm.cuh - the warp-specialised tcgen05 contraction core shared by every FLCE kernel.
+// gemm.cuh - the single-SM warp-specialised tcgen05 contraction core, and what it shares with
+// the CTA-pair core of gemm_pair.cuh: the problem and tile description (two problems per
+// launch, raster groups, fixed-stride or counter-driven tile order), the tile queue depth, the
+// per-warp store staging size and the host launch helpers.
 //
 // One CTA per SM, persistent over output tiles of BM x BN = 128 x 256 (one tcgen05.mma shape,
 // M = 128 rows in the 128 TMEM lanes, N = 256 fp32 columns). Six warps:
@@ -7,7 +10,9 @@
 //   warp 1      : MMA issuer    - one thread issues tcgen05.mma into one of two TMEM
 //                                 accumulators (2 x 256 columns) and commits to mbarriers
 //   warps 2..5  : epilogue      - 128 threads, one accumulator row (TMEM lane) each, drain the
-//                                 accumulator of tile j while the MMAs of tile j+1 run
+//                                 accumulator of tile j while the MMAs of tile j+1 run; each
+//                                 warp owns kEpiStageBytes of shared memory after the ring for
+//                                 transposing its global stores into coalesced ones
 // The contraction itself (D = A . B^T over K) is all this file knows; what happens to a
 // finished tile (online log-sum-exp, dz formation, gradient stores) is the Epi policy.
 //
