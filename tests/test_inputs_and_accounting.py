@@ -63,3 +63,26 @@ def test_kernelindex_dram_floor_reproduced():
 def test_flop_counts():
     assert roofline.flops(16384, 4096, 128256) == 8 * 16384 * 4096 * 128256
     assert roofline.flops(1, 1, 1, "fwd") == 2 and roofline.flops(1, 1, 1, "bwd") == 6
+
+
+def test_traffic_digest_ignores_comments_but_not_code():
+    """bench.py keys the recorded ncu DRAM traffic by a digest of the kernel sources without
+    comments and whitespace: editing a comment keeps the record, editing code voids it."""
+    import bench
+    code = 'int a = 1; // note\n/* block\n comment */ const char* s = "//x/*y*/"; char c = \'"\';\n'
+    assert bench.strip_comments(code) == 'inta=1;constchar*s="//x/*y*/";charc=\'"\';'
+    strip = bench.strip_comments
+    assert strip(code.replace("// note", "// another note")) == strip(code)
+    assert strip(code.replace("a = 1", "a = 2")) != strip(code)
+    assert strip(code.replace('"//x/*y*/"', '"//x/*z*/"')) != strip(code)  # inside a literal
+    # the digest reads the kernel sources through the same stripping
+    sources = {}
+
+    def read(name):
+        import os
+        with open(os.path.join(bench.CSRC, name), encoding="utf-8") as f:
+            sources[name] = f.read()
+        return sources[name] + "\n// an added comment\n"
+
+    assert bench.sources_digest(read) == bench.sources_digest()
+    assert sources and len(bench.sources_digest()) == 64
