@@ -201,3 +201,57 @@ def test_single_call_chunk_rule(lib):
         assert c % 256 == 0 and c >= 256
         assert c <= -(-T // 2 // 256) * 256 + 256 and c < T
         assert c == 256 or 2 * c * ldz <= 1 << 31
+
+
+def _fb(**kw):
+    a = dict(x=FAKE, weight=FAKE + 0x10000000, target=FAKE + 0x20000000, T=64, H=64, V=512,
+             dtype=0, reduction=1, grad_loss=FAKE + 0x22000000, loss=FAKE + 0x23000000,
+             lse=FAKE + 0x23001000, grad_x=FAKE + 0x30000000, grad_weight=FAKE + 0x31000000,
+             workspace=FAKE + 0x40000000, workspace_bytes=1 << 30, status=FAKE + 0x32000000,
+             stream=0)
+    a.update(kw)
+    return B.flce_forward_backward(a["x"], a["weight"], a["target"], a["T"], a["H"], a["V"],
+                                   a["dtype"], a["reduction"], a["grad_loss"], a["loss"],
+                                   a["lse"], a["grad_x"], a["grad_weight"], a["workspace"],
+                                   a["workspace_bytes"], a["status"], a["stream"], check=False)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=0), B.FLCE_ERR_ARG),
+    (dict(grad_loss=0), B.FLCE_ERR_ARG),
+    (dict(grad_weight=0), B.FLCE_ERR_ARG),
+    (dict(status=0), B.FLCE_ERR_ARG),
+    (dict(T=0), B.FLCE_ERR_ARG),
+    (dict(dtype=2), B.FLCE_ERR_ARG),
+    (dict(reduction=3), B.FLCE_ERR_ARG),
+    (dict(H=60), B.FLCE_ERR_UNSUPPORTED),                     # 120-byte bf16 rows
+    (dict(grad_x=FAKE + 0x30000008), B.FLCE_ERR_UNSUPPORTED),  # misaligned output
+    (dict(workspace=0), B.FLCE_ERR_WORKSPACE),
+    (dict(workspace_bytes=64), B.FLCE_ERR_WORKSPACE),
+    (dict(workspace=FAKE + 0x40000010), B.FLCE_ERR_UNSUPPORTED),  # not 256-byte aligned
+    (dict(loss=FAKE + 0x23001004), B.FLCE_ERR_ALIAS),          # loss inside lse
+    (dict(grad_x=FAKE + 0x10), B.FLCE_ERR_ALIAS),              # grad_x over x
+    (dict(workspace=FAKE + 0x31000000), B.FLCE_ERR_ALIAS),     # workspace over grad_weight
+    # 'none': the loss is [T] = 256 bytes, so at 0xF80 it reaches lse (a scalar would not)
+    (dict(reduction=2, loss=FAKE + 0x23000F80), B.FLCE_ERR_ALIAS),
+    (dict(status=FAKE + 0x22000000), B.FLCE_ERR_ALIAS),        # status over grad_loss (input)
+])
+def test_single_call_validation(lib, kw, code):
+    """flce_forward_backward checks every argument before it touches the device (every case
+    here fails validation, so no device work is ever enqueued on the fake addresses)."""
+    assert _fb(**kw) == code
+
+
+
+def test_static_scratch_size_checks_on_host(lib):
+    """flce_forward_static_scratch checks the problem against its fixed scratch size first."""
+    rc = B.flce_forward_static_scratch(FAKE, FAKE + 0x10000000, FAKE + 0x20000000, 0, 64, 512,
+                                       B.FLCE_DTYPE_BF16, B.FLCE_REDUCTION_MEAN, FAKE + 0x30000000,
+                                       FAKE + 0x30001000, FAKE + 0x30000100, 0, check=False)
+    assert rc == B.FLCE_ERR_ARG
+    rc = B.flce_forward_static_scratch(FAKE, FAKE + 0x10000000, FAKE + 0x20000000, 32768, 4096,
+                                       128256, B.FLCE_DTYPE_BF16, B.FLCE_REDUCTION_MEAN,
+                                       FAKE + 0x30000000, FAKE + 0x30001000, FAKE + 0x30000100, 0,
+                                       check=False)
+    assert rc == B.FLCE_ERR_WORKSPACE
+    assert B.flce_forward_workspace_size(16384, 4096, 128256, B.FLCE_DTYPE_BF16) <= 64 << 20
