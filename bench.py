@@ -137,24 +137,33 @@ def recorded_traffic(role: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling during the timed region."""
+    """nvidia-smi clock/throttle sampling during the timed region: samples every 100 ms,
+    timestamped, of which those inside the window marked by begin()/end() are kept."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)  # let the sampler produce its first rows before the timed region
         except OSError:
             self.proc = None
+
+    def begin(self):
+        self.t0 = time.time()
+
+    def end(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
@@ -165,25 +174,27 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            r = [c.strip() for c in r]
-            if len(r) < 8:
+        import datetime
+        rows = []
+        for r in out.strip().splitlines():
+            r = [c.strip() for c in r.split(",")]
+            if len(r) < 9:
                 continue
             try:
-                sm.append(float(r[0]))
-                smax.append(float(r[1]))
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(r[1]), float(r[2]), r[5:9]))
             except ValueError:
                 continue
-            for n, v in zip(names, r[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        inside = [r for r in rows
+                  if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        if not use:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {n for r in use for n, v in zip(names, r[3]) if v.lower() == "active"}
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": sorted(reasons),
+                "samples": len(use), "in_timed_window": bool(inside)}
 
 
 # ------------------------------------------------------------------------------ reference arm
@@ -358,6 +369,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
     barrier()
     torch.cuda.synchronize(dev)
+    clocks.begin()
     ev[0].record(stream)
     for k in range(args.steps):
         B.flce_forward(x.data_ptr(), w.data_ptr(), y.data_ptr(), T, H, V, dt_code, red,
@@ -369,6 +381,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
                         bwd_ws, status.data_ptr(), sp)
         ev[2 * k + 2].record(stream)
     torch.cuda.synchronize(dev)
+    clocks.end()
     barrier()
     clk = clocks.stop()
     B.flce_timing_enable(False)
@@ -570,7 +583,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
