@@ -33,7 +33,8 @@ constexpr int kThreads = 192;
 // Shared memory each epilogue warp owns for transposing its stores (32 rows x 64 bytes).
 constexpr uint32_t kEpiStageBytes = 2048;
 constexpr int kEpiWarp0 = 2;
-constexpr uint32_t kTmemCols = 512;  // two 256-column fp32 accumulators
+constexpr uint32_t kTmemCols = 512;  // all of TMEM: two 256-column fp32 accumulators, or one
+                                     // accumulator of two 256-column halves (wide pair tiles)
 
 // One contraction D[M][N] = A . B^T of a launch. A launch carries one or two problems; their
 // tiles form one list (problem 0 first) that the persistent CTAs walk with a fixed stride.
