@@ -37,7 +37,8 @@ constexpr uint32_t kTmemCols = 512;  // all of TMEM: two 256-column fp32 accumul
                                      // accumulator of two 256-column halves (wide pair tiles)
 
 // One contraction D[M][N] = A . B^T of a launch. A launch carries one or two problems; their
-// tiles form one list (problem 0 first) that the persistent CTAs walk with a fixed stride.
+// tiles form one list (problem 0 first) that the persistent CTAs walk with a fixed stride or,
+// with a tile counter, take in list order as they become free.
 struct GemmProblem {
   int m_tiles;     // ceil(M / tile rows)
   int n_tiles;     // ceil(N / 256)
