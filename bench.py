@@ -444,7 +444,7 @@ def run_ours(args, wl, rank: int, world: int, dist):
     # Every step copies its x, weight and target from pinned host memory and reads its loss
     # back; the copies of step k+1 run on a second stream into the other of two device input
     # sets while step k computes (the set is reused only after the step that read it is done).
-    e2e_steps = max(2, min(args.steps, 6))
+    e2e_steps = max(2, min(args.steps, 20))
     bufs = [(x, w, y), (torch.empty_like(x), torch.empty_like(w), torch.empty_like(y))]
     copy_stream = torch.cuda.Stream(dev)
     h_loss = torch.empty(e2e_steps, dtype=torch.float32).pin_memory()
