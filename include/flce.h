@@ -27,8 +27,8 @@
  * with fp32 accumulation. lse, loss and grad_loss are float32 in both cases.
  *
  * Ownership. The caller owns every buffer, including the workspace and the device status word;
- * the library allocates no device memory. Inputs are never written ("No mutation or aliasing",
- * KernelIndex "Semantics"): an output that overlaps an input or another output is rejected with
+ * the library allocates no device memory. Inputs are never written (KernelIndex "Semantics": inputs
+ * are neither modified nor aliased): an output that overlaps an input or another output is rejected with
  * FLCE_ERR_ALIAS.
  *
  * Asynchrony. Both compute calls only enqueue work on `stream` (a cudaStream_t; NULL means the
@@ -135,7 +135,7 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
  * usual case for a training loss: grad_loss = 1). The Liger-Kernel approach discussed in "[example]
  * fused_linear_cross_entropy kernel" (Helion PR #1268) computes the gradients inside the forward
  * over token chunks; "feat(FLCE): add helion version of fused linear cross entropy"
- * (Liger-Kernel PR #928) calls its chunk-materialised backward "works fine". Here the logits of a
+ * (Liger-Kernel PR #928) reports its chunk-materialised backward as sound. Here the logits of a
  * chunk of tokens (at most half of all tokens and at most 2 GiB of bf16) are computed once and
  * turned into dz in place, so the call does 6 T H V FLOPs instead of the 8 T H V of
  * flce_forward + flce_backward, at the price of the chunk buffer and an fp32 grad_weight

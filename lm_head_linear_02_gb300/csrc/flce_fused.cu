@@ -1,8 +1,9 @@
 // flce_fused.cu - forward and backward in one call, over chunks of tokens, without recomputing
-// the logits (the "compute the gradients during the forward" schedule of the Liger-Kernel
-// discussion in "[example] fused_linear_cross_entropy kernel", Helion PR #1268, and of
-// "feat(FLCE): add helion version of fused linear cross entropy", Liger-Kernel PR #928: "chunk
-// backward (recompute chunk logits then accumulate dx and dw)"; here nothing is recomputed).
+// the logits. The Liger schedule discussed in "[example] fused_linear_cross_entropy kernel"
+// (Helion PR #1268) produces the gradients while the forward runs, and "feat(FLCE): add helion
+// version of fused linear cross entropy" (Liger-Kernel PR #928) describes its chunked backward,
+// which computes each chunk's logits again before accumulating both gradients; here a chunk's
+// logits are computed once and kept for its backward.
 //
 // Per chunk of Tc tokens (never all T: the chunk buffer holds at most half the tokens' logits):
 //   1. logits  : z = x_c . W^T (tcgen05), kept as bf16 z - m_tile plus lse partials (LogitsEpi)

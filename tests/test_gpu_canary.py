@@ -5,7 +5,7 @@ every output buffer and the workspace are carved out of a larger allocation whos
 a byte pattern, the calls run on shapes ragged against every tile size (token rows not a
 multiple of the 32-row store blocks, hidden and vocabulary sizes not multiples of the 256-wide
 tiles), and afterwards the margins must be intact and the inputs bit-identical
-("No mutation or aliasing", KernelIndex "Semantics").
+(KernelIndex "Semantics": inputs are neither modified nor aliased).
 """
 import numpy as np
 import pytest
