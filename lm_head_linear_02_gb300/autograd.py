@@ -39,6 +39,22 @@ def _prep(x: torch.Tensor, weight: torch.Tensor, target: torch.Tensor):
     return x.contiguous(), weight.contiguous(), target.contiguous(), T, H, V, _DTYPES[x.dtype]
 
 
+def _saved_lse(lse: torch.Tensor, T: int, device) -> torch.Tensor:
+    """The forward's lse as the backward reads it: T fp32 values on the device of x. The C
+    entry point cannot see the buffer's length, so a short one is refused here."""
+    if lse.device != device:
+        raise ValueError("lse must be on the device of x")
+    if lse.dim() != 1 or lse.shape[0] != T:
+        raise ValueError(f"lse must have shape [{T}] (one value per token)")
+    return lse.to(torch.float32).contiguous()
+
+
+def _reduction(name: str) -> int:
+    if name not in ("sum", "mean", "none"):
+        raise ValueError(f"reduction must be 'sum', 'mean' or 'none', not {name!r}")
+    return B.reduction_code(name)
+
+
 def _stream(device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
@@ -58,6 +74,7 @@ def flce_forward(x, weight, target, reduction: str = "mean", status: torch.Tenso
     """Enqueue the forward on the current stream. Returns (loss, lse[T], status[1]); loss has
     one element, or T (the per-token losses) for reduction 'none'."""
     x, weight, target, T, H, V, dt = _prep(x, weight, target)
+    red = _reduction(reduction)
     dev = x.device
     ws_bytes = B.flce_forward_workspace_size(T, H, V, dt)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -66,7 +83,7 @@ def flce_forward(x, weight, target, reduction: str = "mean", status: torch.Tenso
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     B.flce_forward(x.data_ptr(), weight.data_ptr(), target.data_ptr(), T, H, V, dt,
-                   B.reduction_code(reduction), loss.data_ptr(), lse.data_ptr(), ws.data_ptr(),
+                   red, loss.data_ptr(), lse.data_ptr(), ws.data_ptr(),
                    ws_bytes, status.data_ptr(), _stream(dev))
     return loss, lse, status
 
@@ -76,8 +93,9 @@ def flce_backward(x, weight, target, lse, grad_loss, reduction: str = "mean",
     """Enqueue the backward on the current stream. Returns (grad_x, grad_weight, status).
     grad_loss has one element, or one per token for reduction 'none'."""
     x, weight, target, T, H, V, dt = _prep(x, weight, target)
+    red = _reduction(reduction)
     dev = x.device
-    lse = lse.to(torch.float32).contiguous()
+    lse = _saved_lse(lse, T, dev)
     n = T if reduction == "none" else 1
     grad_loss = grad_loss.reshape(n).to(device=dev, dtype=torch.float32).contiguous()
     ws_bytes = B.flce_backward_workspace_size(T, H, V, dt)
@@ -87,7 +105,7 @@ def flce_backward(x, weight, target, lse, grad_loss, reduction: str = "mean",
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     B.flce_backward(x.data_ptr(), weight.data_ptr(), target.data_ptr(), lse.data_ptr(), T, H, V,
-                    dt, B.reduction_code(reduction), grad_loss.data_ptr(), grad_x.data_ptr(),
+                    dt, red, grad_loss.data_ptr(), grad_x.data_ptr(),
                     grad_w.data_ptr(), ws.data_ptr(), ws_bytes, status.data_ptr(), _stream(dev))
     return grad_x, grad_w, status
 
@@ -98,6 +116,7 @@ def flce_forward_backward(x, weight, target, grad_loss, reduction: str = "mean",
     advance (one element, or one per token for 'none'). Returns (loss, lse, grad_x,
     grad_weight, status)."""
     x, weight, target, T, H, V, dt = _prep(x, weight, target)
+    red = _reduction(reduction)
     dev = x.device
     n = T if reduction == "none" else 1
     grad_loss = grad_loss.reshape(n).to(device=dev, dtype=torch.float32).contiguous()
@@ -110,7 +129,7 @@ def flce_forward_backward(x, weight, target, grad_loss, reduction: str = "mean",
     if status is None:
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     B.flce_forward_backward(x.data_ptr(), weight.data_ptr(), target.data_ptr(), T, H, V, dt,
-                            B.reduction_code(reduction), grad_loss.data_ptr(), loss.data_ptr(),
+                            red, grad_loss.data_ptr(), loss.data_ptr(),
                             lse.data_ptr(), grad_x.data_ptr(), grad_w.data_ptr(), ws.data_ptr(),
                             ws_bytes, status.data_ptr(), _stream(dev))
     return loss, lse, grad_x, grad_w, status

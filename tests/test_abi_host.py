@@ -161,6 +161,32 @@ def test_binding_raises_on_error(lib):
     assert e.value.code == B.FLCE_ERR_ARG
 
 
+def test_wrapper_refuses_what_the_c_entry_points_cannot_check():
+    """The saved lse's length and device, and the reduction name, are checked in the PyTorch
+    wrapper before any buffer is allocated or the library is called."""
+    torch = pytest.importorskip("torch")
+    from lm_head_linear_02_gb300 import autograd as A
+
+    cpu = torch.device("cpu")
+    ok = A._saved_lse(torch.zeros(6, dtype=torch.float64), 6, cpu)
+    assert ok.dtype == torch.float32 and ok.shape == (6,)
+    for bad in (torch.zeros(5), torch.zeros(7), torch.zeros(6, 1), torch.zeros(())):
+        with pytest.raises(ValueError):
+            A._saved_lse(bad, 6, cpu)
+    with pytest.raises(ValueError):
+        A._saved_lse(torch.zeros(6), 6, torch.device("cuda", 0))
+    assert A._reduction("sum") == B.FLCE_REDUCTION_SUM
+    assert A._reduction("mean") == B.FLCE_REDUCTION_MEAN
+    assert A._reduction("none") == B.FLCE_REDUCTION_NONE
+    for bad in ("avg", "Mean", ""):
+        with pytest.raises(ValueError):
+            A._reduction(bad)
+    # tensors that are not on a CUDA device are refused before anything else happens
+    x, w, y = torch.zeros(4, 8), torch.zeros(16, 8), torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(ValueError):
+        A.flce_forward(x, w, y, "mean")
+
+
 def test_tuning_knobs_validate(lib):
     assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_ROWS) == 2048
     for key, bad in [(B.FLCE_TUNE_RASTER_ROWS, 100), (B.FLCE_TUNE_RASTER_ROWS, 0),
