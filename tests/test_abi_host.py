@@ -281,3 +281,22 @@ def test_static_scratch_size_checks_on_host(lib):
                                        check=False)
     assert rc == B.FLCE_ERR_WORKSPACE
     assert B.flce_forward_workspace_size(16384, 4096, 128256, B.FLCE_DTYPE_BF16) <= 64 << 20
+
+
+def test_plain_c_caller(lib, tmp_path):
+    """include/flce.h compiles as strict C99 and a C program linked against libflce.so gets the
+    documented answers from the size queries and the argument checks (no GPU involved)."""
+    import shutil
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    pkg = os.path.dirname(B.lib_path())
+    exe = str(tmp_path / "c_abi_host_check")
+    src = os.path.join(ROOT, "tests", "c_abi_host_check.c")
+    build = subprocess.run([cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                            "-I", os.path.join(ROOT, "include"), src, "-o", exe, "-L", pkg,
+                            "-lflce", "-Wl,-rpath," + pkg], capture_output=True, text=True)
+    assert build.returncode == 0, build.stderr
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", run.stdout + run.stderr
