@@ -20,7 +20,7 @@ vocabulary or Zipf-distributed with exponent 1.1 (rank 1 = id 0).
 
 Every array comes from ``numpy.random.Generator(PCG64)`` seeded with ``1000 + index`` of the
 workload, one spawned child stream per tensor (x, weight, target). PCG64 is platform independent,
-so the host and the GPU machine produce identical bytes.
+so x86-64 and aarch64 hosts produce identical bytes.
 """
 from __future__ import annotations
 
