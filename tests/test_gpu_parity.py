@@ -18,7 +18,7 @@ import oracle  # noqa: E402
 from lm_head_linear_02_gb300 import autograd as A  # noqa: E402
 from lm_head_linear_02_gb300 import binding as B  # noqa: E402
 from lm_head_linear_02_gb300 import build as build_mod  # noqa: E402
-from lm_head_linear_02_gb300.inputs import make_inputs  # noqa: E402
+from lm_head_linear_02_gb300.inputs import bf16_bits_to_f32, bf16_round_bits, make_inputs  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -212,6 +212,61 @@ def test_targets_at_vocab_edges():
     inp = make_inputs("ragged", T=300, dtype="bf16", seed=3)
     inp.target[:] = np.where(np.arange(300) % 2 == 0, 0, 9999)
     assert_full_parity(inp, "sum", label="edge targets")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_identical_weight_rows_with_large_logits(dtype):
+    """Every weight row equals one vector w0, so all logits of token t equal z_t = x_t.w0
+    (here up to a few thousand in magnitude). Then lse_t = z_t + ln V, every per-token loss is
+    ln V, grad_x = 0 and grad_W[v] = g (sum_t x_t / V - sum_{t: y_t = v} x_t): closed forms,
+    the same case the oracle is pinned on. exp() of such logits overflows fp32 unless the row
+    maximum is taken out first; V = 1000 also leaves a partly masked last vocabulary tile."""
+    T, H, V = 300, 64, 1000
+    r = np.random.default_rng(21)
+    x = (r.standard_normal((T, H)) * 100.0).astype(np.float32)
+    w0 = np.where(r.random(H) < 0.5, -1.0, 1.0).astype(np.float32)
+    w = np.tile(w0, (V, 1))
+    y = r.integers(0, V, size=T).astype(np.int64)
+    if dtype == "bf16":
+        xb = bf16_round_bits(x)
+        x = bf16_bits_to_f32(xb)
+        xd = torch.from_numpy(xb.view(np.int16)).cuda().view(torch.bfloat16)
+        wd = torch.from_numpy(bf16_round_bits(w).view(np.int16)).cuda().view(torch.bfloat16)
+    else:
+        xd, wd = torch.from_numpy(x).cuda(), torch.from_numpy(w).cuda()
+    loss, lse, gx, gw = run_gpu(xd, wd, torch.from_numpy(y).cuda(), "mean")
+    x64 = x.astype(np.float64)
+    z = x64 @ w0.astype(np.float64)
+    assert np.abs(z).max() > 1000.0
+    g = 1.0 / T
+    # lse carries the contraction's rounding of z (fp32 sums of H terms; 3xTF32 operands), which
+    # scales with sum_h |x_th w0_h|; each per-token loss lse_t - z_t reuses the same z and must
+    # come out as ln V
+    scale = np.abs(x64).sum(1)
+    assert np.all(np.abs(lse - (z + math.log(V))) <= 4e-6 * scale + 2e-4)
+    assert abs(loss - math.log(V)) / math.log(V) <= TOL[dtype]["loss"]
+    # sum_v dz[t, v] = g (sum_v p - 1) must vanish; an lse off by a lot would leave g |w0|
+    assert np.abs(gx).max() <= 0.05 * g
+    expect_gw = np.tile(g * x64.sum(0) / V, (V, 1))
+    np.add.at(expect_gw, y, -g * x64)
+    assert norm_err(gw, expect_gw) <= TOL[dtype]["grad"]
+    ref = oracle.flce(x64, w.astype(np.float64), y, "mean")
+    assert norm_err(gw, ref["grad_weight"]) <= TOL[dtype]["grad"]
+
+
+def test_wrapper_refuses_a_short_or_host_lse():
+    inp = make_inputs("tiny", T=64, H=64, V=512, dtype="bf16", seed=2)
+    x, w, y = to_device(inp)
+    loss, lse, status = A.flce_forward(x, w, y, "mean")
+    g = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        A.flce_backward(x, w, y, lse[:-1], g, "mean")
+    with pytest.raises(ValueError):
+        A.flce_backward(x, w, y, lse.cpu(), g, "mean")
+    with pytest.raises(ValueError):
+        A.flce_forward(x, w, y, "average")
+    torch.cuda.synchronize()
+    A.check_status(status)
 
 
 def test_out_of_range_target_sets_status_and_nan_loss():
