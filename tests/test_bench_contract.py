@@ -1,0 +1,60 @@
+"""bench.py's command line and JSON line, checked on the CPU through its reference arm.
+
+The reference arm times the float64 oracle on a token sample on the host cores, so it runs
+without a GPU; these tests run it on the tiny workload and check the line's keys and values,
+that non-zero ranks stay silent, and that fewer than three warm-up steps are refused.
+"""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+BENCH = os.path.join(ROOT, "bench.py")
+
+
+def _run(args, env_extra=None):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run([sys.executable, BENCH] + args, cwd=ROOT, env=env,
+                          capture_output=True, text=True, timeout=300)
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = _run(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3",
+              "--oracle-tokens", "16"])
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    # tokens per second over the timed steps: 16 tokens per step
+    assert abs(d["value"] - 16 * 1e3 / d["ms_per_step"]) <= 1e-6 * d["value"]
+    assert d["config"]["workload"] == "tiny"
+    assert d["config"]["tokens"] == 128 and d["config"]["vocab"] == 2048
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert "16 tokens" in cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_is_silent_on_other_ranks():
+    r = _run(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"],
+             {"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
+
+
+def test_fewer_than_three_warmup_steps_are_refused():
+    r = _run(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "2"])
+    assert r.returncode == 2
+    assert "--warmup must be >= 3" in r.stderr
