@@ -8,6 +8,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 from lm_head_linear_02_gb300 import binding as B
@@ -300,3 +301,50 @@ def test_plain_c_caller(lib, tmp_path):
     assert build.returncode == 0, build.stderr
     run = subprocess.run([exe], capture_output=True, text=True, timeout=60)
     assert run.returncode == 0 and run.stdout.strip() == "ok", run.stdout + run.stderr
+
+
+def test_sizing_rules_hold_on_random_shapes(lib):
+    """The slab, chunk and workspace sizes for 300 random shapes (log-uniform T and V, both
+    dtypes): 256-column granularity, no empty slab or chunk, the 1 GiB slab and 2 GiB chunk
+    budgets, as few slabs as the budget allows, slabs and chunks of nearly equal size, and
+    workspaces that hold what the kernels write (for bf16, nothing more than that)."""
+    r = np.random.default_rng(2024)
+    budget_slab, budget_chunk = 1 << 30, 1 << 31
+    up = lambda a, b: -(-a // b) * b  # noqa: E731
+    for _ in range(300):
+        T = int(np.exp(r.uniform(0, np.log(1 << 18))))
+        V = int(np.exp(r.uniform(0, np.log(1 << 19))))
+        H = 8 * int(r.integers(1, 2049))
+        for dt in (B.FLCE_DTYPE_BF16, B.FLCE_DTYPE_F32):
+            label = f"T={T} H={H} V={V} dtype={dt}"
+            vc = B.flce_backward_slab_width(T, H, V, dt)
+            n = -(-V // vc)
+            per_col = 2 * T if dt == B.FLCE_DTYPE_BF16 else 16 * up(T, 4)
+            vc_max = max(256, budget_slab // per_col // 256 * 256)
+            assert vc % 256 == 0 and 256 <= vc <= up(V, 256), label
+            assert (n - 1) * vc < V <= n * vc, label
+            assert vc <= vc_max, label
+            assert n == 1 or up(-(-V // (n - 1)), 256) > vc_max, label  # no fewer slabs fit
+            assert vc - (V - (n - 1) * vc) <= 256 * n, label             # nearly equal widths
+            bws = B.flce_backward_workspace_size(T, H, V, dt)
+            if dt == B.FLCE_DTYPE_BF16:
+                need = 2 * T * vc + (4 * T * H if n > 1 else 0)
+                assert need <= bws <= need + 4096, label
+            else:
+                assert bws >= 8 * T * vc + 4 * vc * up(T, 4) * 2, label
+            fws = B.flce_forward_workspace_size(T, H, V, dt)
+            nt = -(-V // 256)
+            assert 8 * nt * T + 4 * T <= fws, label
+            c = B.flce_forward_backward_chunk_tokens(T, H, V, dt)
+            if dt != B.FLCE_DTYPE_BF16 or T < 512:
+                assert c == T, label
+                continue
+            k = -(-T // c)
+            ldz = up(V, 256)
+            assert c % 256 == 0 and 256 <= c < T, label
+            assert (k - 1) * c < T <= k * c, label
+            assert c <= up(-(-T // 2), 256), label
+            assert c == 256 or 2 * c * ldz <= budget_chunk, label
+            assert c - (T - (k - 1) * c) <= 256 * k, label
+            fbs = B.flce_forward_backward_workspace_size(T, H, V, dt)
+            assert fbs >= 2 * c * ldz + (4 * V * H if k > 1 else 0), label
