@@ -348,3 +348,23 @@ def test_sizing_rules_hold_on_random_shapes(lib):
             assert c - (T - (k - 1) * c) <= 256 * k, label
             fbs = B.flce_forward_backward_workspace_size(T, H, V, dt)
             assert fbs >= 2 * c * ldz + (4 * V * H if k > 1 else 0), label
+
+
+def test_missing_library_fails_loudly(lib, monkeypatch, tmp_path):
+    """Without libflce.so every call raises FlceNotBuilt: there is no fallback path."""
+    monkeypatch.setattr(B, "_LIB", None)
+    monkeypatch.setattr(B, "lib_path", lambda: str(tmp_path / "libflce.so"))
+    with pytest.raises(B.FlceNotBuilt):
+        B.flce_version()
+    with pytest.raises(B.FlceNotBuilt):
+        B.flce_forward_workspace_size(16, 64, 512, B.FLCE_DTYPE_BF16)
+
+
+def test_build_is_current_and_covers_every_source(lib):
+    """build() leaves a library newer than every source, header and the public header, and the
+    build inputs include every .cu and .cuh/.h file of the source directory."""
+    assert build_mod.up_to_date()
+    names = {os.path.basename(f) for f in build_mod._inputs()}
+    on_disk = {f for f in os.listdir(build_mod.CSRC) if f.endswith((".cu", ".cuh", ".h"))}
+    assert on_disk <= names
+    assert "flce.h" in names
