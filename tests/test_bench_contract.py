@@ -58,3 +58,21 @@ def test_fewer_than_three_warmup_steps_are_refused():
     r = _run(["--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "2"])
     assert r.returncode == 2
     assert "--warmup must be >= 3" in r.stderr
+
+
+def test_cpu_baseline_times_at_least_the_bounded_duration():
+    """The CPU baseline repeats token samples of the workload until its minimum duration has
+    passed and reports tokens per second over all of them."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from lm_head_linear_02_gb300.inputs import make_inputs
+
+    inp = make_inputs("tiny")
+    cb = bench.cpu_baseline(inp, 48, min_seconds=0.3)
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["cores"] >= 1
+    done = int(cb["sample"].split()[0])
+    secs = float(cb["sample"].rsplit(",", 1)[1].split()[0])
+    assert done >= 48 and done % 48 == 0 and "samples of 48" in cb["sample"]
+    elapsed = done / cb["value"]
+    assert elapsed >= 0.3
+    assert abs(elapsed - secs) <= 0.051  # the sample text prints the seconds to 0.1
