@@ -10,6 +10,7 @@ from .flce_oracle import (  # noqa: F401
     flce,
     forward,
     grad_scale,
+    grad_weight_rows,
     log_sum_exp,
     logits,
     sampled_rows,

@@ -57,6 +57,7 @@ __all__ = [
     "backward",
     "flce",
     "sampled_rows",
+    "grad_weight_rows",
 ]
 
 REDUCTIONS = ("sum", "mean", "none")
@@ -176,3 +177,35 @@ def sampled_rows(x, weight, target, rows, reduction: str = "mean", grad_loss=1.0
     dz = dlogits(z, lse, target_rows, g)
     return {"lse": lse, "per_token_loss": per_token, "grad_x": dz @ weight}
 
+
+
+def grad_weight_rows(x, weight, target, lse, vocab_rows, reduction: str = "mean",
+                     grad_loss=1.0, chunk: int = 4096):
+    """grad_weight[v, :] for selected vocabulary rows v only, given the forward's lse.
+
+    Written out from the definition (Helion PR #1268, backward): for one vocabulary row v,
+    column v of the logits is z[:, v] = x . weight[v], column v of dz is
+    (exp(z[:, v] - lse) - [target == v]) * g, and grad_weight[v] = sum_t dz[t, v] * x[t].
+    Each row needs only its own logits column and the per-token lse, so a full-size problem can
+    be checked one vocabulary row at a time. Tokens are taken in chunks (memory only), summed in
+    increasing token order.
+    """
+    x, weight, target = _check(x, weight, target)
+    lse = np.asarray(lse, dtype=np.float64).reshape(-1)
+    rows = np.asarray(vocab_rows, dtype=np.int64).reshape(-1)
+    T = x.shape[0]
+    if lse.shape != (T,):
+        raise ValueError("lse needs one value per token")
+    if rows.size and (rows.min() < 0 or rows.max() >= weight.shape[0]):
+        raise ValueError("vocab row outside [0, vocab)")
+    g = grad_scale(grad_loss, reduction, T)
+    out = np.zeros((rows.size, x.shape[1]), dtype=np.float64)
+    for t0 in range(0, T, chunk):
+        t1 = min(T, t0 + chunk)
+        zc = logits(x[t0:t1], weight[rows])                   # [chunk, rows]: logit columns
+        dzc = np.exp(zc - lse[t0:t1, None])
+        dzc -= (target[t0:t1, None] == rows[None, :])         # one-hot of the target column
+        gc = g[t0:t1] if isinstance(g, np.ndarray) else g
+        dzc *= (gc[:, None] if isinstance(gc, np.ndarray) else gc)
+        out += dzc.T @ x[t0:t1]
+    return out

@@ -215,6 +215,48 @@ def _grad_x_negated(monkeypatch):
     _plant(monkeypatch, "backward", backward)
 
 
+def _gw_rows_with(dz_column):
+    """The oracle's grad_weight_rows with its dz columns formed by dz_column(z, lse, onehot, g)."""
+    def grad_weight_rows(x, weight, target, lse, vocab_rows, reduction="mean", grad_loss=1.0,
+                         chunk=4096):
+        x, weight, target = OM._check(x, weight, target)
+        lse = np.asarray(lse, dtype=np.float64).reshape(-1)
+        rows = np.asarray(vocab_rows, dtype=np.int64).reshape(-1)
+        T = x.shape[0]
+        g = OM.grad_scale(grad_loss, reduction, T)
+        out = np.zeros((rows.size, x.shape[1]))
+        for t0 in range(0, T, chunk):
+            t1 = min(T, t0 + chunk)
+            zc = OM.logits(x[t0:t1], weight[rows])
+            onehot = (target[t0:t1, None] == rows[None, :]).astype(np.float64)
+            gc = g[t0:t1, None] if isinstance(g, np.ndarray) else g
+            out += dz_column(zc, lse[t0:t1, None], onehot, gc).T @ x[t0:t1]
+        return out
+    return grad_weight_rows
+
+
+def _gw_rows_sign_flipped(monkeypatch):
+    _plant(monkeypatch, "grad_weight_rows",
+           _gw_rows_with(lambda z, lse, oh, g: -(np.exp(z - lse) - oh) * g))
+
+
+def _gw_rows_without_onehot(monkeypatch):
+    _plant(monkeypatch, "grad_weight_rows", _gw_rows_with(lambda z, lse, oh, g: np.exp(z - lse) * g))
+
+
+def _gw_rows_onehot_at_neighbour(monkeypatch):
+    _plant(monkeypatch, "grad_weight_rows",
+           _gw_rows_with(lambda z, lse, oh, g: (np.exp(z - lse) - np.roll(oh, 1, axis=1)) * g))
+
+
+def _gw_rows_without_upstream_gradient(monkeypatch):
+    _plant(monkeypatch, "grad_weight_rows", _gw_rows_with(lambda z, lse, oh, g: np.exp(z - lse) - oh))
+
+
+def _gw_rows_without_lse(monkeypatch):
+    _plant(monkeypatch, "grad_weight_rows", _gw_rows_with(lambda z, lse, oh, g: (np.exp(z) - oh) * g))
+
+
 MUTANTS = {
     "log-sum-exp without the row maximum": _lse_without_max,
     "log-sum-exp in base 2": _lse_base_two,
@@ -233,13 +275,18 @@ MUTANTS = {
     "grad_weight overwritten per token chunk": _grad_weight_overwritten,
     "grad_x negated": _grad_x_negated,
     "grad_weight from token-reversed x": _grad_weight_from_wrong_operand,
+    "sampled grad_weight rows with the dz sign flipped": _gw_rows_sign_flipped,
+    "sampled grad_weight rows without the one-hot term": _gw_rows_without_onehot,
+    "sampled grad_weight rows with the one-hot at the neighbouring row": _gw_rows_onehot_at_neighbour,
+    "sampled grad_weight rows without the upstream gradient": _gw_rows_without_upstream_gradient,
+    "sampled grad_weight rows without the lse": _gw_rows_without_lse,
 }
 
 
 def test_unmutated_oracle_passes_every_pin_through_the_runner():
     failed, passed = _run_pins()
     assert not failed, failed
-    assert len(passed) >= 30  # every pin and its parametrisations ran
+    assert len(passed) >= 35  # every pin and its parametrisations ran
 
 
 @pytest.mark.parametrize("name", list(MUTANTS))

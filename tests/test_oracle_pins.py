@@ -353,3 +353,57 @@ def test_none_reduction_sampled_rows_and_shape_check():
     assert np.allclose(s["per_token_loss"], full["loss"][rows], rtol=0, atol=1e-15)
     with pytest.raises(ValueError):
         oracle.backward(x, w, y, full["lse"], "none", grad_loss=np.ones(T - 1))
+
+
+# ---------------------------------------------------------------- sampled grad_weight rows
+
+def test_grad_weight_rows_zero_weight_closed_form():
+    """weight = 0 and lse = ln V given from the closed form, not from the oracle's forward:
+    grad_weight[v] = g (sum_t x_t / V - sum_{t: y_t = v} x_t)."""
+    T, H, V = 9, 4, 13
+    x, _, y = _rand_case(T, H, V, seed=20)
+    y[:3] = 5  # a row that several tokens target
+    w = np.zeros((V, H))
+    rows = np.array([5, 0, 12, 7])
+    got = oracle.grad_weight_rows(x, w, y, np.full(T, math.log(V)), rows, "mean", grad_loss=2.0,
+                                  chunk=4)
+    g = 2.0 / T
+    for i, v in enumerate(rows):
+        expect = g * (x.sum(0) / V - x[y == v].sum(0))
+        assert np.allclose(got[i], expect, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("reduction", ["sum", "mean", "none"])
+def test_grad_weight_rows_against_torch(reduction):
+    """Library special case: torch float64 cross_entropy + autograd on materialised logits; the
+    helper gets torch's own logsumexp as its lse, so nothing of the oracle's forward is used."""
+    torch = pytest.importorskip("torch")
+    T, H, V = 23, 9, 31
+    x, w, y = _rand_case(T, H, V, seed=21)
+    y[::4] = 3
+    u = np.random.default_rng(22).standard_normal(T)
+    gl = u if reduction == "none" else 1.3
+    xt = torch.tensor(x, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    per = torch.nn.functional.cross_entropy(xt @ wt.T, torch.tensor(y), reduction=reduction)
+    (per * torch.tensor(gl, dtype=torch.float64)).sum().backward()
+    lse_t = torch.logsumexp(xt.detach() @ wt.detach().T, dim=1).numpy()
+    rows = np.array([3, 0, V - 1, 17, 3])
+    got = oracle.grad_weight_rows(x, w, y, lse_t, rows, reduction, grad_loss=gl, chunk=5)
+    assert np.allclose(got, wt.grad.numpy()[rows], rtol=1e-11, atol=1e-14)
+
+
+def test_grad_weight_rows_match_full_backward_and_finite_differences():
+    T, H, V = 6, 3, 7
+    x, w, y = _rand_case(T, H, V, seed=23)
+    full = oracle.flce(x, w, y, "sum", grad_loss=0.8)
+    rows = np.arange(V)
+    got = oracle.grad_weight_rows(x, w, y, full["lse"], rows, "sum", grad_loss=0.8, chunk=2)
+    assert np.allclose(got, full["grad_weight"], rtol=1e-13, atol=1e-15)
+    eps = 1e-6
+    for v, h in [(y[0], 0), (1, 2), (V - 1, 1)]:
+        wp, wm = w.copy(), w.copy()
+        wp[v, h] += eps
+        wm[v, h] -= eps
+        fd = 0.8 * (oracle.forward(x, wp, y, "sum")[0] - oracle.forward(x, wm, y, "sum")[0]) / (2 * eps)
+        assert abs(got[v, h] - fd) < 1e-7
