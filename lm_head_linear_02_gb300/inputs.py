@@ -18,6 +18,16 @@ The pages ship no datasets; these synthetic draws stand in for the benchmark scr
 activations and weights: x ~ N(0, 1), weight ~ N(0, 0.02^2), and targets either uniform over the
 vocabulary or Zipf-distributed with exponent 1.1 (rank 1 = id 0).
 
+Two further recipes put the softmax where a trained LM head has it, which the near-uniform
+softmax of weight ~ N(0, 0.02^2) never reaches (the Helion PR #1268 discussion upcasts bf16
+logits to fp32 for this regime):
+
+* a wide logit spread: weight ~ N(0, w_std^2) with a larger w_std (0.3 at hidden 1024 gives
+  logits of standard deviation ~10, so a few columns of each row carry most of the softmax);
+* confident predictions: after the draws, weight[target[t]] += margin * x[t] / |x[t]|^2 for
+  every token (x already rounded to the input dtype), so that the target logit of each token
+  stands `margin` above its drawn value and its probability approaches 1 (loss near 0).
+
 Every array comes from ``numpy.random.Generator(PCG64)`` seeded with ``1000 + index`` of the
 workload, one spawned child stream per tensor (x, weight, target). PCG64 is platform independent,
 so x86-64 and aarch64 hosts produce identical bytes.
@@ -54,6 +64,7 @@ class Workload:
     x_std: float = 1.0
     w_std: float = 0.02
     zipf_s: float = 1.1
+    confident_margin: float = 0.0  # > 0: raise each token's target logit by this much
     note: str = field(default="", compare=False)
 
     @property
@@ -80,6 +91,14 @@ WORKLOADS = {
                  note="Qwen3-sized head"),
         Workload("gemma3_head_t8192", 7, 8192, 2304, 262208, "bf16", "uniform", ("mean",),
                  note="Gemma3-sized head: narrow hidden, very wide vocabulary"),
+        Workload("spread", 8, 1100, 1024, 8000, "bf16", "uniform", ("sum", "mean", "none"),
+                 w_std=0.3, note="logits of standard deviation ~10: a peaked softmax"),
+        Workload("confident", 9, 1100, 1024, 8000, "bf16", "uniform", ("sum", "mean", "none"),
+                 confident_margin=14.0,
+                 note="target probability ~0.99, loss ~1e-2"),
+        Workload("spread_confident", 10, 1100, 1024, 8000, "bf16", "uniform",
+                 ("sum", "mean", "none"), w_std=0.3, confident_margin=60.0,
+                 note="logits spread over tens of units and a dominant target"),
     ]
 }
 
@@ -138,8 +157,9 @@ def _draw_normal(rng: np.random.Generator, shape, std: float) -> np.ndarray:
 
 def make_inputs(workload: Workload | str, T: int | None = None, H: int | None = None,
                 V: int | None = None, dtype: str | None = None,
-                target_dist: str | None = None, seed: int | None = None) -> FlceInputs:
-    """Generate the seeded inputs of a workload; T/H/V/dtype/target_dist/seed override it."""
+                target_dist: str | None = None, seed: int | None = None,
+                w_std: float | None = None, confident_margin: float | None = None) -> FlceInputs:
+    """Generate the seeded inputs of a workload; the keyword arguments override its fields."""
     if isinstance(workload, str):
         workload = WORKLOADS[workload]
     T = workload.T if T is None else int(T)
@@ -148,8 +168,10 @@ def make_inputs(workload: Workload | str, T: int | None = None, H: int | None = 
     dtype = workload.dtype if dtype is None else dtype
     target_dist = workload.target_dist if target_dist is None else target_dist
     seed = workload.seed if seed is None else int(seed)
+    w_std = workload.w_std if w_std is None else float(w_std)
+    margin = workload.confident_margin if confident_margin is None else float(confident_margin)
     wl = Workload(workload.name, workload.index, T, H, V, dtype, target_dist,
-                  workload.reductions, workload.x_std, workload.w_std, workload.zipf_s,
+                  workload.reductions, workload.x_std, w_std, workload.zipf_s, margin,
                   workload.note)
 
     child = np.random.SeedSequence(seed).spawn(3)
@@ -163,12 +185,21 @@ def make_inputs(workload: Workload | str, T: int | None = None, H: int | None = 
     else:
         raise ValueError(f"unknown target distribution {target_dist!r}")
 
+    if dtype not in ("bf16", "f32"):
+        raise ValueError(f"unknown dtype {dtype!r}")
     xb = wb = None
     if dtype == "bf16":
         xb = bf16_round_bits(x)
-        wb = bf16_round_bits(w)
         x = bf16_bits_to_f32(xb)
+    if margin > 0.0:
+        # raise each target logit by `margin` (relative to the x both paths see); tokens that
+        # share a target add their shifts to the same weight row
+        x64 = x.astype(np.float64)
+        shift = margin * x64 / np.einsum("th,th->t", x64, x64)[:, None]
+        w64 = w.astype(np.float64)
+        np.add.at(w64, y, shift)
+        w = w64.astype(np.float32)
+    if dtype == "bf16":
+        wb = bf16_round_bits(w)
         w = bf16_bits_to_f32(wb)
-    elif dtype != "f32":
-        raise ValueError(f"unknown dtype {dtype!r}")
     return FlceInputs(wl, x, w, y, xb, wb)

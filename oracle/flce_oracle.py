@@ -42,6 +42,9 @@ Pins (tests/test_oracle_pins.py): closed forms for weight = 0, x = 0 and identic
 a hand-derived 2x2x3 example (tests/golden/), brute-force pure-Python loops, torch's float64
 cross_entropy as a library special case, central finite differences, the two-class logistic
 special case, row sums of dz, shift invariance, sum = T * mean, and chunk-size independence.
+The per-row helpers (sampled_rows, grad_weight_rows) are pinned against the full oracle, and
+grad_weight_rows also against the weight = 0 closed form with lse given in closed form, torch's
+float64 autograd with torch's own logsumexp, and finite differences.
 """
 from __future__ import annotations
 
