@@ -165,14 +165,23 @@ int flce_forward_backward(const void* x, const void* weight, const int64_t* targ
  * start-up and which may not call cudaMalloc while it runs (cudaMalloc can also synchronise the
  * device). This call computes exactly what flce_forward computes, with the same arguments minus
  * the workspace, and allocates nothing: its scratch is one file-scope device array of
- * FLCE_STATIC_SCRATCH_BYTES that every GPU loading the library holds until the process exits.
+ * FLCE_STATIC_SCRATCH_BYTES, part of the library's device code.
+ *   - The array is reserved in a CUDA context when the library's module holding it is loaded
+ *     there; with CUDA's default lazy module loading that is this call's first use in the
+ *     context, and the reservation lasts until the context is destroyed or the process exits.
+ *     A caller with a fixed budget should make one small call at start-up, so that this
+ *     reservation (which fails with FLCE_ERR_CUDA when the device is out of memory) happens then.
  *   - Returns FLCE_ERR_WORKSPACE, enqueuing nothing, when the problem's forward scratch
- *     (flce_forward_workspace_size) exceeds FLCE_STATIC_SCRATCH_BYTES; bf16 problems up to
- *     about T = 16700 tokens at V = 128256 fit.
- *   - All calls on a device share the array and it keeps the last call's contents; nothing in
+ *     (flce_forward_workspace_size) exceeds FLCE_STATIC_SCRATCH_BYTES. bf16 problems up to
+ *     about T = 16700 tokens fit at V = 128256. fp32 problems also hold TF32 hi/lo copies of x
+ *     and weight there, 8 (T + V) H bytes plus the per-tile partials, so only small fp32
+ *     problems fit (T = 1269, H = 1000, V = 10000 needs about 90 MB and is rejected).
+ *   - All calls in a context share the array and it keeps the last call's contents; nothing in
  *     it has to start at zero. Calls whose GPU work overlaps (e.g. on unordered streams) race.
- *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
+ *   - The array's device address is looked up (cudaGetSymbolAddress) with the caller's context
+ *     current, once per CUDA context, and cached under that context's unique id, so a context
+ *     created by the caller or a device's primary context created again after a reset gets its
+ *     own lookup. Make the first call in each context before any stream capture.
  */
 int flce_forward_static_scratch(const void* x, const void* weight, const int64_t* target,
                                 int64_t T, int64_t H, int64_t V, int dtype, int reduction,

@@ -55,15 +55,20 @@ int main(void) {
   check(flce_forward_backward(NULL, NULL, NULL, T, H, V, FLCE_DTYPE_BF16, FLCE_REDUCTION_SUM,
                               NULL, NULL, NULL, NULL, NULL, NULL, 0, NULL, NULL) == FLCE_ERR_ARG,
         "flce_forward_backward with null pointers");
-  /* the fixed scratch is checked against the problem first: T = 0 is invalid, and 32768
-   * tokens at V = 128256 need more than FLCE_STATIC_SCRATCH_BYTES */
-  check(flce_forward_static_scratch(NULL, NULL, NULL, 0, H, V, FLCE_DTYPE_BF16,
+  /* the fixed scratch is checked against the problem before any CUDA call: null pointers and
+   * T = 0 are invalid, and 32768 tokens at V = 128256 need more than FLCE_STATIC_SCRATCH_BYTES
+   * (the stand-in addresses below are never dereferenced) */
+  check(flce_forward_static_scratch(NULL, NULL, NULL, T, H, V, FLCE_DTYPE_BF16,
                                     FLCE_REDUCTION_MEAN, &loss, NULL, NULL, NULL) == FLCE_ERR_ARG,
+        "flce_forward_static_scratch with null pointers");
+  check(flce_forward_static_scratch(&loss, &loss, &raster, 0, H, V, FLCE_DTYPE_BF16,
+                                    FLCE_REDUCTION_MEAN, &loss, &loss, &failures, NULL) ==
+            FLCE_ERR_ARG,
         "flce_forward_static_scratch with T = 0");
   check(flce_forward_workspace_size(2 * T, H, V, FLCE_DTYPE_BF16) > FLCE_STATIC_SCRATCH_BYTES,
         "forward scratch of 32768 tokens above the static array");
-  check(flce_forward_static_scratch(NULL, NULL, NULL, 2 * T, H, V, FLCE_DTYPE_BF16,
-                                    FLCE_REDUCTION_MEAN, &loss, NULL, NULL, NULL) ==
+  check(flce_forward_static_scratch(&loss, &loss, &raster, 2 * T, H, V, FLCE_DTYPE_BF16,
+                                    FLCE_REDUCTION_MEAN, &loss, &loss, &failures, NULL) ==
             FLCE_ERR_WORKSPACE,
         "flce_forward_static_scratch above its scratch size");
 

@@ -282,6 +282,21 @@ def test_static_scratch_size_checks_on_host(lib):
                                        check=False)
     assert rc == B.FLCE_ERR_WORKSPACE
     assert B.flce_forward_workspace_size(16384, 4096, 128256, B.FLCE_DTYPE_BF16) <= 64 << 20
+    # fp32 problems keep their TF32 hi/lo copies of x and weight in the scratch too, 8 (T + V) H
+    # bytes: the ragged fp32 workload (1269 x 1000 x 10000) needs about 90 MB and is rejected
+    need = B.flce_forward_workspace_size(1269, 1000, 10000, B.FLCE_DTYPE_F32)
+    assert need >= 8 * (1269 + 10000) * 1000 > 64 << 20
+    rc = B.flce_forward_static_scratch(FAKE, FAKE + 0x10000000, FAKE + 0x20000000, 1269, 1000,
+                                       10000, B.FLCE_DTYPE_F32, B.FLCE_REDUCTION_MEAN,
+                                       FAKE + 0x30000000, FAKE + 0x30001000, FAKE + 0x30000100, 0,
+                                       check=False)
+    assert rc == B.FLCE_ERR_WORKSPACE
+    assert B.flce_forward_workspace_size(128, 256, 2048, B.FLCE_DTYPE_F32) <= 64 << 20
+    # a null output is refused before the size check or any CUDA call
+    rc = B.flce_forward_static_scratch(FAKE, FAKE + 0x10000000, FAKE + 0x20000000, 128, 256, 2048,
+                                       B.FLCE_DTYPE_BF16, B.FLCE_REDUCTION_MEAN, 0,
+                                       FAKE + 0x30001000, FAKE + 0x30000100, 0, check=False)
+    assert rc == B.FLCE_ERR_ARG
 
 
 def test_plain_c_caller(lib, tmp_path):
