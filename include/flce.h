@@ -216,10 +216,25 @@ int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_RO
  *                          128-row CTA tiles but leaves no TMEM for overlapping a tile's
  *                          epilogue with the next tile. A bit mask of FLCE_ROLE_*; -1 (the
  *                          default) picks a measured mask. Roles not on SM pairs ignore it.
+ *   FLCE_TUNE_RASTER_VOCAB vocabulary rows per raster group of the contractions whose N
+ *                          dimension is the vocabulary (the forward projection, the backward's
+ *                          dz and the single call's chunk logits): tiles sweep the token rows
+ *                          inside a group, so the group's weight rows stay in L2 while x streams
+ *                          past. Multiple of 256; 0 (the default) rasters those contractions
+ *                          over token rows as well (FLCE_TUNE_RASTER_ROWS).
+ *   FLCE_TUNE_SPLIT_EPILOGUE which roles on wide pair tiles drain each finished 128-row block
+ *                          with two epilogue warps of 128 columns each (16 epilogue warps per
+ *                          CTA) instead of one of 256: the single accumulator of a wide tile is
+ *                          released sooner, at the price of fewer registers per thread. A bit mask
+ *                          of FLCE_ROLE_FORWARD (forward projection and single-call chunk
+ *                          logits) and FLCE_ROLE_DZ; FLCE_ROLE_GRADS is ignored. -1 restores
+ *                          the default (FLCE_ROLE_FORWARD | FLCE_ROLE_DZ).
  * Read at each launch. Returns FLCE_OK or FLCE_ERR_ARG. */
 #define FLCE_TUNE_RASTER_ROWS 1
 #define FLCE_TUNE_SM_PAIRS 2
 #define FLCE_TUNE_WIDE_TILES 3
+#define FLCE_TUNE_RASTER_VOCAB 4
+#define FLCE_TUNE_SPLIT_EPILOGUE 5
 #define FLCE_ROLE_FORWARD 1
 #define FLCE_ROLE_DZ 2
 #define FLCE_ROLE_GRADS 4

@@ -15,10 +15,21 @@ namespace flce {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ void load_chunk(uint32_t taddr, int c, float (&v)[32]) {
+// Columns [32c, 32c + 32) of this warp's rows of the finished tile: one accumulator, or the
+// fp32 sum of the large and the correction accumulator (3xTF32 path).
+__device__ __forceinline__ void load_chunk(const EpiCtx& ctx, int c, float (&v)[32]) {
   __syncwarp();  // tcgen05.ld is .sync.aligned: the whole warp issues it together
   uint32_t r[32];
-  tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
+  tmem_ld32(ctx.taddr + static_cast<uint32_t>(c * 32), r);
+  if (ctx.two_acc) {  // uniform
+    uint32_t q[32];
+    tmem_ld32(ctx.taddr_corr + static_cast<uint32_t>(c * 32), q);
+    tmem_ld_wait(r);
+    tmem_ld_wait(q);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) + __uint_as_float(q[j]);
+    return;
+  }
   tmem_ld_wait(r);
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
@@ -104,6 +115,10 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
 // Each (vocab tile, token) pair leaves a partial (max m, sum of exp(z - m)) that the combine
 // kernel merges in a fixed order; the one tile holding target[t] also writes z[t, target[t]].
 // Vocab columns >= V are masked to -inf.
+// A tile's partial is formed from its two 128-column halves (chunks 0-3 and 4-7), each folded
+// chunk by chunk, then merged: half 1 into half 0. One warp does both halves, or two warps one
+// each (split 2, half 1 passed to half 0's warp through the exchange slots); the arithmetic,
+// and so every bit of the result, is the same either way.
 struct FwdEpi {
   struct Args {
     const int64_t* target;
@@ -115,20 +130,18 @@ struct FwdEpi {
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
 
-  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
-                                              uint32_t taddr, uint4* stage) {
-    const int t = mb * kBM + row;
-    const bool valid = t < a.T;
-    const int n0 = nb * kBN;
-    const long long y = valid ? static_cast<long long>(a.target[t]) : -1ll;
-    const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
-    float m = -INFINITY, s = 0.f, zy = 0.f;
+  // Fold chunks [c_begin, c_end) of the tile into (m, s); picks up the target logit.
+  static __device__ __forceinline__ void fold(const Args& a, const EpiCtx& ctx, int n0, int rel,
+                                              int c_begin, int c_end, float& m, float& s,
+                                              float& zy) {
+    m = -INFINITY;
+    s = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = c_begin; c < c_end; ++c) {
       const int c0 = n0 + c * 32;
       if (c0 >= a.V) break;  // uniform across the warp
       float v[32];
-      load_chunk(taddr, c, v);
+      load_chunk(ctx, c, v);
       if (c0 + 32 > a.V) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -159,28 +172,68 @@ struct FwdEpi {
       s = s * ex2((m - mn) * kLog2e) + ((s0 + s1) + (s2 + s3));
       m = mn;
     }
-    if (valid) {
+  }
+
+  // (m0, s0) <- the merge of half 0's and half 1's partials (half 1 may be empty: -inf, 0)
+  static __device__ __forceinline__ void merge(float& m0, float& s0, float m1, float s1) {
+    const float mn = fmaxf(m0, m1);
+    s0 = s0 * ex2((m0 - mn) * kLog2e) + s1 * ex2((m1 - mn) * kLog2e);
+    m0 = mn;
+  }
+
+  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb,
+                                              const EpiCtx& ctx) {
+    const int t = mb * kBM + ctx.row;
+    const bool valid = t < a.T;
+    const int n0 = nb * kBN;
+    const long long y = valid ? static_cast<long long>(a.target[t]) : -1ll;
+    const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
+    constexpr int kHalfChunks = kBN / 64;
+    float zy = 0.f;
+    float m, s;
+    if (ctx.split == 1) {
+      float m1, s1;
+      fold(a, ctx, n0, rel, 0, kHalfChunks, m, s, zy);
+      fold(a, ctx, n0, rel, kHalfChunks, 2 * kHalfChunks, m1, s1, zy);
+      merge(m, s, m1, s1);
+    } else {
+      fold(a, ctx, n0, rel, ctx.c_begin, ctx.c_end, m, s, zy);
+      float2* slot = ctx.xchg + 32 * (ctx.iter & 1);
+      const int lane = ctx.row & 31;
+      if (ctx.part == 1) {
+        slot[lane] = make_float2(m, s);
+        mbar_arrive(ctx.xbar);
+      } else {
+        if (!mbar_wait(ctx.xbar, static_cast<uint32_t>(ctx.iter & 1), ctx.status, ctx.abort))
+          return;  // the partner left on the abort path: outputs are undefined anyway
+        const float2 o = slot[lane];
+        merge(m, s, o.x, o.y);
+      }
+    }
+    if (valid && ctx.part == 0) {
       const size_t o = static_cast<size_t>(nb) * a.T + t;
       a.part_m[o] = m;
       a.part_s[o] = s;
-      if (rel >= 0) a.zy[t] = zy;
     }
+    if (valid && rel >= ctx.c_begin * 32 && rel < ctx.c_end * 32) a.zy[t] = zy;
   }
 };
 
 // ------------------------------------------------------------------------------- chunk logits
 // Single-call forward + backward over a chunk of tokens (the logits are computed once, not
-// recomputed): like FwdEpi, each (vocab tile, token) pair leaves its (max m, sum of
-// exp(z - m)) partial and the tile holding target[t] writes z[t, target[t]]; in addition the
-// tile's logits are kept, shifted by their tile maximum, as bf16 in a chunk buffer
-// zbuf[t][v] = z[t, v] - m. The shift puts the largest logits of each tile near 0, where bf16
-// is most precise, so exp(zbuf + m - lse) recovers the dominant softmax terms accurately.
-// Two passes over TMEM: the tile maximum first, then the shifted store and the exp-sum.
+// recomputed): like FwdEpi, each (128-column vocab half-tile, token) pair leaves its (max m, sum
+// of exp(z - m)) partial and the tile holding target[t] writes z[t, target[t]]; in addition the
+// half-tile's logits are kept, shifted by their maximum, as bf16 in a chunk buffer
+// zbuf[t][v] = z[t, v] - m. The shift puts the largest logits of each half-tile near 0, where
+// bf16 is most precise, so exp(zbuf + m - lse) recovers the dominant softmax terms accurately.
+// Two passes over each half's TMEM columns: its maximum first, then the shifted store and the
+// exp-sum. One warp does both halves, or two warps one each (split 2); every partial belongs
+// to one half, so nothing is exchanged and the results do not depend on the split.
 struct LogitsEpi {
   struct Args {
     const int64_t* target;  // chunk rows
-    float* part_m;          // [n_tiles][T]
-    float* part_s;          // [n_tiles][T]
+    float* part_m;          // [2 n_tiles][T]: one partial per 128-column half-tile
+    float* part_s;          // [2 n_tiles][T]
     float* zy;              // [T]
     __nv_bfloat16* zbuf;    // [T][ldz]
     int ldz;
@@ -189,20 +242,17 @@ struct LogitsEpi {
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
 
-  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
-                                              uint32_t taddr, uint4* stage) {
-    const int t = mb * kBM + row;
-    const bool valid = t < a.T;
+  static __device__ __forceinline__ void half(const Args& a, const EpiCtx& ctx, int t, bool valid,
+                                              int nb, int rel, int h) {
+    constexpr int kHalfChunks = kBN / 64;
     const int n0 = nb * kBN;
-    const long long y = valid ? static_cast<long long>(a.target[t]) : -1ll;
-    const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
     float m = -INFINITY, zy = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = h * kHalfChunks; c < (h + 1) * kHalfChunks; ++c) {
       const int c0 = n0 + c * 32;
       if (c0 >= a.V) break;  // uniform across the warp
       float v[32];
-      load_chunk(taddr, c, v);
+      load_chunk(ctx, c, v);
       const int q = rel - c * 32;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -213,11 +263,11 @@ struct LogitsEpi {
     const float ml = m * kLog2e;
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = h * kHalfChunks; c < (h + 1) * kHalfChunks; ++c) {
       const int c0 = n0 + c * 32;
       if (c0 >= a.V) break;
       float v[32];
-      load_chunk(taddr, c, v);
+      load_chunk(ctx, c, v);
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const float e0 = ex2(fmaf(v[j], kLog2e, -ml));
@@ -227,13 +277,29 @@ struct LogitsEpi {
         v[j] -= m;
         v[j + 1] -= m;
       }
-      store_rows_bf16x32(stage, v, row & 31, a.zbuf + c0, a.ldz, t - (row & 31), a.T);
+      store_rows_bf16x32(ctx.stage, v, ctx.row & 31, a.zbuf + c0, a.ldz, t - (ctx.row & 31),
+                         a.T);
     }
     if (valid) {
-      const size_t o = static_cast<size_t>(nb) * a.T + t;
+      const size_t o = static_cast<size_t>(2 * nb + h) * a.T + t;
       a.part_m[o] = m;
       a.part_s[o] = s0 + s1;
-      if (rel >= 0) a.zy[t] = zy;
+      if (rel >= h * 128 && rel < (h + 1) * 128) a.zy[t] = zy;
+    }
+  }
+
+  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb,
+                                              const EpiCtx& ctx) {
+    const int t = mb * kBM + ctx.row;
+    const bool valid = t < a.T;
+    const int n0 = nb * kBN;
+    const long long y = valid ? static_cast<long long>(a.target[t]) : -1ll;
+    const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
+    if (ctx.split == 1) {
+      half(a, ctx, t, valid, nb, rel, 0);
+      half(a, ctx, t, valid, nb, rel, 1);
+    } else {
+      half(a, ctx, t, valid, nb, rel, ctx.part);
     }
   }
 };
@@ -263,8 +329,10 @@ struct DzEpi {
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
 
-  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb, int row,
-                                              uint32_t taddr, uint4* stage) {
+  static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb,
+                                              const EpiCtx& ctx) {
+    const int row = ctx.row;
+    uint4* stage = ctx.stage;
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
     const float lsel = valid ? __ldg(a.lse + t) * kLog2e : 0.f;
@@ -274,11 +342,11 @@ struct DzEpi {
     const long long rel = y - a.slab0 - n0;
     const bool unit_scale = a.row_scale == nullptr;  // uniform: sum / mean reductions
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = ctx.c_begin; c < ctx.c_end; ++c) {
       const int c0 = n0 + c * 32;
       if (c0 >= a.slab_w) break;  // uniform
       float v[32];
-      load_chunk(taddr, c, v);
+      load_chunk(ctx, c, v);
       if (unit_scale && c0 + 32 <= a.slab_w) {
         // The common case: every column inside the slab and row factor 1, so only the one
         // target column of a row (if it lies in this chunk) differs from exp(z - lse).
@@ -344,18 +412,20 @@ struct GradWEpi {
     st.g = a.grad_loss ? __ldg(a.grad_loss) * a.scale : a.scale;
   }
 
-  static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
-                                              uint32_t taddr, uint4* stage) {
+  static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb,
+                                              const EpiCtx& ctx) {
+    const int row = ctx.row;
+    uint4* stage = ctx.stage;
     const int r = mb * kBM + row;  // slab-relative vocab row
     const bool valid = r < a.slab_w;
     const size_t vrow = static_cast<size_t>(a.slab0) + r;
     const int lane = row & 31;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = ctx.c_begin; c < ctx.c_end; ++c) {
       const int h0 = nb * kBN + c * 32;
       if (h0 >= a.H) break;
       float v[32];
-      load_chunk(taddr, c, v);
+      load_chunk(ctx, c, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= st.g;
       if constexpr (kF32Out) {
@@ -411,8 +481,10 @@ struct GradXEpi {
     st.g = a.grad_loss ? __ldg(a.grad_loss) * a.scale : a.scale;
   }
 
-  static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb, int row,
-                                              uint32_t taddr, uint4* stage) {
+  static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb,
+                                              const EpiCtx& ctx) {
+    const int row = ctx.row;
+    uint4* stage = ctx.stage;
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
     if constexpr (!kF32Out) {
@@ -423,11 +495,11 @@ struct GradXEpi {
       const int qa = lane >> 2, qb = lane & 3;
       const int t0 = t - lane;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = ctx.c_begin; c < ctx.c_end; ++c) {
         const int h0 = nb * kBN + c * 32;
         if (h0 >= a.H) break;
         float v[32];
-        load_chunk(taddr, c, v);
+        load_chunk(ctx, c, v);
         // both 16-column halves through shared memory first, then every accumulator load of
         // the chunk in flight at once, then the adds and stores
         uint4 out[2][4];
@@ -483,11 +555,11 @@ struct GradXEpi {
       }
     } else {  // fp32 outputs (the TF32 path): plain per-row stores
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = ctx.c_begin; c < ctx.c_end; ++c) {
         const int h0 = nb * kBN + c * 32;
         if (h0 >= a.H) break;
         float v[32];
-        load_chunk(taddr, c, v);
+        load_chunk(ctx, c, v);
         if (!valid) continue;
         const int n = min(32, a.H - h0);
         const size_t o = static_cast<size_t>(t) * a.H + h0;

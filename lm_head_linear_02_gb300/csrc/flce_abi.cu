@@ -77,11 +77,15 @@ bool make_tmap_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uin
 
 namespace {
 std::atomic<int> g_tune_raster_rows{2048};
+std::atomic<int> g_tune_raster_vocab{kDefaultRasterVocab};
+std::atomic<int> g_tune_split_epilogue{kDefaultSplitEpilogue};
 std::atomic<int> g_tune_sm_pairs{-1};
 std::atomic<int> g_tune_wide_tiles{-1};
 }  // namespace
 
 int tune_raster_rows() { return g_tune_raster_rows.load(); }
+int tune_raster_vocab() { return g_tune_raster_vocab.load(); }
+int tune_split_epilogue() { return g_tune_split_epilogue.load(); }
 
 namespace {
 std::atomic<int> g_withhold_request{0};
@@ -310,7 +314,7 @@ size_t carve_fused(Carver& c, int64_t T, int64_t H, int64_t V, FusedWs* w) {
   r.rows = fused_chunk_rows(T, V);
   r.ldz = round_up(V, kTileN);
   r.n_chunks = cdiv(T, r.rows);
-  const int64_t nt = r.ldz / kTileN;
+  const int64_t nt = r.ldz / (kTileN / 2);  // one partial per 128-column half-tile
   r.zbuf = static_cast<__nv_bfloat16*>(c.take(size_t(2) * r.rows * r.ldz));
   r.part_m = static_cast<float*>(c.take(sizeof(float) * nt * r.rows));
   r.part_s = static_cast<float*>(c.take(sizeof(float) * nt * r.rows));
@@ -433,6 +437,15 @@ int flce_set_tuning(int key, int64_t value) {
       if (value < -1 || value > 7) return FLCE_ERR_ARG;
       flce::g_tune_sm_pairs.store(static_cast<int>(value));
       return FLCE_OK;
+    case FLCE_TUNE_RASTER_VOCAB:
+      if (value < 0 || value > (int64_t(1) << 24) || value % 256 != 0) return FLCE_ERR_ARG;
+      flce::g_tune_raster_vocab.store(static_cast<int>(value));
+      return FLCE_OK;
+    case FLCE_TUNE_SPLIT_EPILOGUE:
+      if (value < -1 || value > 7) return FLCE_ERR_ARG;
+      flce::g_tune_split_epilogue.store(value < 0 ? flce::kDefaultSplitEpilogue
+                                                  : static_cast<int>(value));
+      return FLCE_OK;
     case FLCE_TUNE_WIDE_TILES:
       if (value < -1 || value > 7) return FLCE_ERR_ARG;
       flce::g_tune_wide_tiles.store(static_cast<int>(value));
@@ -447,6 +460,12 @@ int flce_get_tuning(int key, int64_t* value) {
   switch (key) {
     case FLCE_TUNE_RASTER_ROWS:
       *value = flce::g_tune_raster_rows.load();
+      return FLCE_OK;
+    case FLCE_TUNE_RASTER_VOCAB:
+      *value = flce::g_tune_raster_vocab.load();
+      return FLCE_OK;
+    case FLCE_TUNE_SPLIT_EPILOGUE:
+      *value = flce::g_tune_split_epilogue.load();
       return FLCE_OK;
     case FLCE_TUNE_SM_PAIRS: {
       flce::Device dev;
@@ -794,7 +813,7 @@ int flce_forward_backward(const void* x, const void* weight, const int64_t* targ
     e = flce::timed_launch(0, s, [&] { return flce::launch_chunk_logits(tx_k, tw_k, cl); });
     if (e == cudaSuccess)
       e = flce::launch_combine_rows(w.part_m, w.part_s, w.zy, target + t0, int(rows), int(V),
-                                    int(w.ldz / kTileN), lse + t0, w.block_sums + t0 / 256,
+                                    int(w.ldz / (kTileN / 2)), lse + t0, w.block_sums + t0 / 256,
                                     none ? loss + t0 : nullptr, status, s);
     if (e == cudaSuccess) e = flce::launch_form_dz(cl);
     if (e == cudaSuccess)

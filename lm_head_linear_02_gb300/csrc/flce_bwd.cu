@@ -15,9 +15,10 @@ namespace flce {
 template <bool kTF32, class Epi>
 static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ta_lo,
                             const CUtensorMap& tb_lo, int M, int N, int K, int* status, int sms,
-                            cudaStream_t stream, const typename Epi::Args& ea) {
+                            cudaStream_t stream, const typename Epi::Args& ea,
+                            bool vocab_n = false) {
   GemmGrid g{};
-  g.p[0] = make_problem(M, N, K, StageGeom<kTF32>::kBK, false, false, kBM, 0);
+  g.p[0] = make_problem(M, N, K, StageGeom<kTF32>::kBK, false, false, kBM, 0, vocab_n);
   g.num_problems = 1;
   g.status = status;
   return launch_gemm<kTF32, Epi, NoEpi>(ta, tb, ta_lo, tb_lo, g, ea, NoEpi::Args{}, sms, stream);
@@ -29,15 +30,15 @@ cudaError_t launch_dz_bf16(const CUtensorMap& tx, const CUtensorMap& tw_slab, co
   const Core core = role_core(p.sms, FLCE_ROLE_DZ);
   if (core != kCoreSingle) {  // x boxed {64 x core_a_box_rows}, W slab {64 x 128} for this path
     GemmGrid g{};
-    g.p[0] = make_problem(p.T, p.slab_w, p.H, 64, false, false, core_tile_rows(core), 0);
+    g.p[0] = make_problem(p.T, p.slab_w, p.H, 64, false, false, core_tile_rows(core), 0, true);
     g.num_problems = 1;
     g.status = p.status;
     g.tile_counter = p.tile_counter;
-    return launch_pair_core<DzEpi<false>, NoEpi>(core, tx, tw_slab, tx, tw_slab, g, ea,
-                                                 NoEpi::Args{}, p.sms, p.stream);
+    return launch_pair_core<DzEpi<false>, NoEpi, 2>(core, tx, tw_slab, tx, tw_slab, g, ea,
+                                                    NoEpi::Args{}, p.sms, p.stream, FLCE_ROLE_DZ);
   }
   return run_gemm<false, DzEpi<false>>(tx, tw_slab, tx, tw_slab, p.T, p.slab_w, p.H, p.status,
-                                       p.sms, p.stream, ea);
+                                       p.sms, p.stream, ea, true);
 }
 
 cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
@@ -55,7 +56,7 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
                                 p.slab0,
                                 p.slab_w};
   return run_gemm<true, DzEpi<true>>(tx_hi, tw_hi, tx_lo, tw_lo, p.T, p.slab_w, p.H, p.status,
-                                     p.sms, p.stream, ea);
+                                     p.sms, p.stream, ea, true);
 }
 
 // grad_W (A = dz slab, B = x, both MN-major, K = T) and grad_x (A = dz slab K-major, B = W slab
@@ -112,11 +113,11 @@ int pair_roles(int sms) {
     const int d = decided[dev].load();
     if (d) return d - 1;
   }
-  auto kern = k_umma_gemm_pair<256, GradXEpi<false>, GradWEpi<false>>;
+  auto kern = k_umma_gemm_pair<256, 1, GradXEpi<false>, GradWEpi<false>>;
   int mask = 0;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           PairGeom<256>::kSmemBytes) == cudaSuccess)
-    mask = 2 * pair_resident_clusters<256>(kern, sms) >= 2 * (sms / 2) ? kAutoPairRoles : 0;
+                           PairGeom<256, 1>::kSmemBytes) == cudaSuccess)
+    mask = 2 * pair_resident_clusters<256, 1>(kern, sms) >= 2 * (sms / 2) ? kAutoPairRoles : 0;
   else
     cudaGetLastError();
   if (dev >= 0 && dev < 64) decided[dev].store(mask + 1);

@@ -6,7 +6,8 @@
 // logits are computed once and kept for its backward.
 //
 // Per chunk of Tc tokens (never all T: the chunk buffer holds at most half the tokens' logits):
-//   1. logits  : z = x_c . W^T (tcgen05), kept as bf16 z - m_tile plus lse partials (LogitsEpi)
+//   1. logits  : z = x_c . W^T (tcgen05), kept as bf16 z - m (m: the maximum of each 128-column
+//                half-tile) plus lse partials per half-tile (LogitsEpi)
 //   2. combine : lse, per-token loss / loss block sums of the chunk rows (k_fwd_combine)
 //   3. form dz : dz = (exp(z - lse) - onehot) * row scale, in place, bf16 (k_form_dz)
 //   4. grads   : grad_x[chunk] = dz . W (complete, K = V) and grad_W (+)= dz^T . x_c (K = Tc,
@@ -18,8 +19,9 @@
 
 namespace flce {
 
-// dz[t][v] = (exp(zbuf[t][v] + m[v / 256][t] - lse[t]) - [v == target[t]]) * row_scale[t] for
-// v < V, 0 for V <= v < ldz; 8 consecutive columns (16 bytes) per thread, in place.
+// dz[t][v] = (exp(zbuf[t][v] + m[v / 128][t] - lse[t]) - [v == target[t]]) * row_scale[t] for
+// v < V, 0 for V <= v < ldz; 8 consecutive columns (16 bytes) per thread, in place. (m holds
+// one shift per 128-column half-tile, as LogitsEpi stored the logits.)
 __global__ void __launch_bounds__(256)
     k_form_dz(__nv_bfloat16* __restrict__ zbuf, int ldz, int rows, int V,
               const float* __restrict__ part_m, const float* __restrict__ lse,
@@ -30,7 +32,7 @@ __global__ void __launch_bounds__(256)
   const int t = static_cast<int>(idx / vecs);
   const int v0 = static_cast<int>(idx - static_cast<int64_t>(t) * vecs) * 8;
   uint4* p = reinterpret_cast<uint4*>(zbuf + static_cast<size_t>(t) * ldz + v0);
-  const float off = (part_m[static_cast<size_t>(v0 / kBN) * rows + t] - lse[t]) * kLog2e;
+  const float off = (part_m[static_cast<size_t>(v0 / 128) * rows + t] - lse[t]) * kLog2e;
   const long long y = static_cast<long long>(target[t]);
   const float rs = row_scale ? row_scale[t] : 1.0f;
   uint4 w = *p;
@@ -60,13 +62,13 @@ cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
   LogitsEpi::Args ea{c.target, c.part_m, c.part_s, c.zy, c.zbuf, c.ldz, c.rows, c.V};
   const Core core = role_core(c.sms, FLCE_ROLE_FORWARD);  // maps boxed for this core
   GemmGrid g{};
-  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, core_tile_rows(core), 0);
+  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, core_tile_rows(core), 0, true);
   g.num_problems = 1;
   g.status = c.status;
   g.tile_counter = c.tile_counter;  // tiles in list order: the pairs sharing a W tile stay in step
   if (core != kCoreSingle)
-    return launch_pair_core<LogitsEpi, NoEpi>(core, tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{}, c.sms,
-                                              c.stream);
+    return launch_pair_core<LogitsEpi, NoEpi, 2>(core, tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{},
+                                                 c.sms, c.stream, FLCE_ROLE_FORWARD);
   return launch_gemm<false, LogitsEpi, NoEpi>(tx_c, tw, tx_c, tw, g, ea, NoEpi::Args{}, c.sms,
                                               c.stream);
 }

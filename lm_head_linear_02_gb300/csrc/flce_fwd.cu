@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kCombineThreads)
     for (int i = 0; i < n_tiles; ++i) {
       const float m = part_m[static_cast<size_t>(i) * T + t];
       const float s = part_s[static_cast<size_t>(i) * T + t];
+      if (m == -INFINITY) continue;  // an empty partial (a half-tile wholly beyond V)
       const float mn = fmaxf(M, m);
       S = S * ex2((M - mn) * kLog2e) + s * ex2((m - mn) * kLog2e);
       M = mn;
@@ -83,7 +84,7 @@ static cudaError_t launch_forward(const CUtensorMap& tx, const CUtensorMap& tw,
                                   const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
                                   const FwdLaunch& p) {
   GemmGrid g{};
-  g.p[0] = make_problem(p.T, p.V, p.H, StageGeom<kTF32>::kBK, false, false, kBM, 0);
+  g.p[0] = make_problem(p.T, p.V, p.H, StageGeom<kTF32>::kBK, false, false, kBM, 0, true);
   g.num_problems = 1;
   g.status = p.status;
   g.tile_counter = p.tile_counter;
@@ -126,13 +127,13 @@ cudaError_t launch_forward_bf16(const CUtensorMap& tx, const CUtensorMap& tw, co
   const Core core = role_core(p.sms, FLCE_ROLE_FORWARD);
   if (core != kCoreSingle) {  // x boxed {64 x core_a_box_rows}, W {64 x 128} for this path
     GemmGrid g{};
-    g.p[0] = make_problem(p.T, p.V, p.H, 64, false, false, core_tile_rows(core), 0);
+    g.p[0] = make_problem(p.T, p.V, p.H, 64, false, false, core_tile_rows(core), 0, true);
     g.num_problems = 1;
     g.status = p.status;
     g.tile_counter = p.tile_counter;
     FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V};
-    cudaError_t e = launch_pair_core<FwdEpi, NoEpi>(core, tx, tw, tx, tw, g, ea, NoEpi::Args{},
-                                                    p.sms, p.stream);
+    cudaError_t e = launch_pair_core<FwdEpi, NoEpi, 2>(core, tx, tw, tx, tw, g, ea, NoEpi::Args{},
+                                                       p.sms, p.stream, FLCE_ROLE_FORWARD);
     if (e != cudaSuccess) return e;
     return launch_combine(p);
   }

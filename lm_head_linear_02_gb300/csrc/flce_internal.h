@@ -22,7 +22,16 @@ constexpr int kTileN = 256;
 //                       (the default) to decide per device.
 //   tune_wide_tiles(): bit mask of the roles whose CTA pairs use 256-row CTA tiles, or -1 (the
 //                      default: kDefaultWideRoles).
+//   tune_raster_vocab(): vocabulary rows per raster group of the contractions whose N dimension
+//                       is the vocabulary (forward, dz, chunk logits): tiles walk the token
+//                       rows inside a group, so the group's weight rows stay in L2 while x
+//                       streams; 0 rasters those over token rows too.
+//   tune_split_epilogue(): bit mask of the roles (FLCE_ROLE_FORWARD: the forward projection and
+//                       the chunk logits; FLCE_ROLE_DZ) whose wide pair tiles drain each row
+//                       block with two epilogue warps (16 per CTA) instead of one.
 int tune_raster_rows();
+int tune_raster_vocab();
+int tune_split_epilogue();
 int tune_sm_pairs();
 int tune_wide_tiles();
 
@@ -33,6 +42,13 @@ bool take_withhold_request();
 // can be paired: all three (with the wide CTA tiles below; on 128-row CTA tiles dz alone was
 // faster on single SMs).
 constexpr int kAutoPairRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ | FLCE_ROLE_GRADS;
+
+// Default of tune_raster_vocab(): 0, the token-row raster of tune_raster_rows() for every
+// launch.
+constexpr int kDefaultRasterVocab = 0;
+
+// Default of tune_split_epilogue().
+constexpr int kDefaultSplitEpilogue = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ;
 
 // Roles measured faster on 256-row CTA tiles when they run on CTA pairs.
 constexpr int kDefaultWideRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ | FLCE_ROLE_GRADS;
@@ -167,7 +183,7 @@ struct ChunkLaunch {
   float scale;             // 1 or 1/T
   __nv_bfloat16* zbuf;     // [rows][ldz] chunk logits (shifted) / dz
   int ldz;
-  float *part_m, *part_s, *zy;  // [ldz / 256][rows], [ldz / 256][rows], [rows]
+  float *part_m, *part_s, *zy;  // [ldz / 128][rows] (one per half-tile) x 2, [rows]
   void* grad_x_rows;       // grad_x + t0 * H
   void* grad_w;
   float* gw_acc;           // fp32 [V][H] accumulator across chunks

@@ -20,6 +20,12 @@
 // is used for the backward contractions whose reduction runs over tokens or vocab rows.
 // For fp32 inputs (kTF32x3) each operand arrives as a (hi, lo) pair of TF32-exact copies and
 // each K-step issues hi.hi + hi.lo + lo.hi, which carries ~fp32 accuracy on TF32 tensor cores.
+// The tensor core's additions into an fp32 accumulator do not round to nearest (their errors
+// all lean one way) and the error of each is a fraction of the accumulator's last place, so
+// the large hi.hi products and the small correction products go to separate accumulators (the
+// two 256-column halves of TMEM; no double buffering on this path) and the epilogue adds the
+// two in fp32: the large accumulator sees a third of the additions, the small one has tiny
+// last places.
 #pragma once
 
 #include "flce_internal.h"
@@ -44,7 +50,8 @@ struct GemmProblem {
   int n_tiles;     // ceil(N / 256)
   int k_blocks;    // ceil(K / BK)
   int a_mn, b_mn;  // operand majors (1 = MN-major; bf16 only)
-  int group_m;     // raster: tiles walk N inside groups of group_m consecutive M tiles
+  int group_m;     // raster: tiles walk N inside groups of group_m consecutive M tiles ...
+  int group_n;     // ... or, when group_n > 0, walk M inside groups of group_n N tiles
   int tile_begin;  // first linear tile of this problem within the launch
 };
 
@@ -73,16 +80,29 @@ __device__ __forceinline__ TileInfo map_tile(const GemmGrid& g, int t) {
   const int m_tiles = second ? g.p[1].m_tiles : g.p[0].m_tiles;
   const int n_tiles = second ? g.p[1].n_tiles : g.p[0].n_tiles;
   const int group_m = second ? g.p[1].group_m : g.p[0].group_m;
+  const int group_n = second ? g.p[1].group_n : g.p[0].group_n;
   const int r = t - (second ? g.p[1].tile_begin : g.p[0].tile_begin);
-  const int per_group = group_m * n_tiles;
-  const int grp = r / per_group;
-  const int first = grp * group_m;
-  const int gsz = min(group_m, m_tiles - first);
-  const int q = r - grp * per_group;
   TileInfo ti;
   ti.prob = second ? 1 : 0;
-  ti.mb = first + q % gsz;
-  ti.nb = q / gsz;
+  if (group_n > 0) {
+    // groups of group_n consecutive N tiles (their B rows stay in L2); A streams past them,
+    // every N tile of the group taken for one M tile before the next M tile
+    const int per_group = group_n * m_tiles;
+    const int grp = r / per_group;
+    const int first = grp * group_n;
+    const int gsz = min(group_n, n_tiles - first);
+    const int q = r - grp * per_group;
+    ti.mb = q / gsz;
+    ti.nb = first + q % gsz;
+  } else {
+    const int per_group = group_m * n_tiles;
+    const int grp = r / per_group;
+    const int first = grp * group_m;
+    const int gsz = min(group_m, m_tiles - first);
+    const int q = r - grp * per_group;
+    ti.mb = first + q % gsz;
+    ti.nb = q / gsz;
+  }
   ti.k_blocks = second ? g.p[1].k_blocks : g.p[0].k_blocks;
   ti.a_mn = second ? g.p[1].a_mn : g.p[0].a_mn;
   ti.b_mn = second ? g.p[1].b_mn : g.p[0].b_mn;
@@ -104,12 +124,34 @@ struct StageGeom {
   static constexpr uint32_t kSmemBytes = kRingBytes + 1024 + 4 * kEpiStageBytes + 1024;
 };
 
+// What an epilogue warp is given for one finished tile (one 128-row block of accumulators).
+// Its 32 threads own one row each (one TMEM lane) and drain the 32-column chunks
+// [c_begin, c_end) of the block's 256 columns. With split = 2 two warps share the same rows and
+// take the column halves (part 0: chunks 0-3, part 1: chunks 4-7). An epilogue that needs
+// per-row results of both halves passes them from part 1 to part 0 through xchg (two sets of
+// 32 float2 slots, alternating with `iter`, the warp's tile count) and the mbarrier xbar (32
+// arrivals per tile, phase parity iter & 1): part 1 writes and arrives, part 0 waits, bounded
+// like every pipeline wait, so a partner that left on the abort path cannot hang it.
+struct EpiCtx {
+  int row;            // accumulator row of this thread within the 128-row block
+  uint32_t taddr;     // TMEM address of this warp's lane quarter, column 0 of the block
+  uint4* stage;       // this warp's kEpiStageBytes of store staging
+  int c_begin, c_end; // 32-column chunks of the block this warp drains
+  int part, split;    // column half (0 / 1) and warps per row block (1 / 2)
+  int iter;           // tiles this warp has drained before this one
+  int two_acc;        // 1: the tile is the sum of two accumulators, taddr and taddr_corr
+  uint32_t taddr_corr;
+  uint32_t xbar;      // exchange mbarrier of the two warps sharing rows (split 2)
+  float2* xchg;       // exchange slots of those two warps (split 2)
+  int* status;        // device status word (a timed-out exchange sets FLCE_STATUS_TIMEOUT)
+  volatile int* abort;
+};
+
 struct NoEpi {
   struct Args {};
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
-  static __device__ __forceinline__ void tile(const Args&, State&, int, int, int, uint32_t,
-                                              uint4*) {}
+  static __device__ __forceinline__ void tile(const Args&, State&, int, int, const EpiCtx&) {}
 };
 
 // A stage holds [A_hi][A_lo][B_hi][B_lo] (lo copies only for kTF32x3, whose operands are
@@ -284,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, g.status, abort_flag)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        const uint32_t d_corr = tmem_base + static_cast<uint32_t>(kBN);  // kTF32x3: corrections
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, g.status, abort_flag)) {
             ok = false;
@@ -301,9 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
               const uint64_t a_lo = a_hi + (G::kABytes >> 4);
               const uint64_t b_lo = b_hi + (G::kBBytes >> 4);
-              mma_tf32(d_tmem, a_lo, b_hi, idesc, accum);
-              mma_tf32(d_tmem, a_hi, b_lo, idesc, 1u);
-              mma_tf32(d_tmem, a_hi, b_hi, idesc, 1u);
+              mma_tf32(d_corr, a_lo, b_hi, idesc, accum);
+              mma_tf32(d_corr, a_hi, b_lo, idesc, 1u);
+              mma_tf32(d_tmem, a_hi, b_hi, idesc, accum);
             }
           }
           mma_commit(empty_bar(stage));
@@ -317,7 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (g.withhold: the failure-path test leaves CTA 0's first tile unsignalled so that its
         // epilogue's bounded wait runs out.)
         if (!(g.withhold && blockIdx.x == 0 && consumed == k_blocks)) mma_commit(tfull_bar(acc));
-        if (++acc == 2) {
+        if (kTF32x3) {  // one (two-part) accumulator
+          acc_phase ^= 1u;
+        } else if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
@@ -353,15 +398,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       __syncwarp();
       const TileInfo ti = map_tile(g, t);
-      const uint32_t taddr =
+      EpiCtx ctx;
+      ctx.row = row;
+      ctx.taddr =
           tmem_base + static_cast<uint32_t>(acc * kBN) + (static_cast<uint32_t>(quarter * 32) << 16);
+      ctx.stage = stage;
+      ctx.c_begin = 0;
+      ctx.c_end = kBN / 32;
+      ctx.part = 0;
+      ctx.split = 1;
+      ctx.iter = 0;
+      ctx.two_acc = kTF32x3 ? 1 : 0;
+      ctx.taddr_corr = ctx.taddr + static_cast<uint32_t>(kBN);
+      ctx.xbar = 0;
+      ctx.xchg = nullptr;
+      ctx.status = g.status;
+      ctx.abort = abort_flag;
       if (ti.prob == 0)
-        Epi0::tile(e0, st0, ti.mb, ti.nb, row, taddr, stage);
+        Epi0::tile(e0, st0, ti.mb, ti.nb, ctx);
       else
-        Epi1::tile(e1, st1, ti.mb, ti.nb, row, taddr, stage);
+        Epi1::tile(e1, st1, ti.mb, ti.nb, ctx);
       tc_fence_before_sync();
       mbar_arrive(tempty_bar(acc));
-      if (++acc == 2) {
+      if (kTF32x3) {
+        acc_phase ^= 1u;
+      } else if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -394,9 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------- host helpers
 
-// Problem description for a launch; `tile_rows` is 128 for this core, 256 for CTA pairs.
+// Problem description for a launch; `tile_rows` is 128 for this core, 256 or 512 for CTA
+// pairs. `vocab_n`: the N dimension is the vocabulary (B = weight rows), which is rastered in
+// groups of tune_raster_vocab() rows when that is set, instead of groups of M rows.
 inline GemmProblem make_problem(int M, int N, int K, int bk, bool a_mn, bool b_mn, int tile_rows,
-                                int tile_begin) {
+                                int tile_begin, bool vocab_n = false) {
   GemmProblem p;
   p.m_tiles = (M + tile_rows - 1) / tile_rows;
   p.n_tiles = (N + kBN - 1) / kBN;
@@ -405,6 +468,7 @@ inline GemmProblem make_problem(int M, int N, int K, int bk, bool a_mn, bool b_m
   p.b_mn = b_mn ? 1 : 0;
   const int g = tune_raster_rows() / tile_rows;
   p.group_m = g > 0 ? g : 1;
+  p.group_n = vocab_n ? tune_raster_vocab() / kBN : 0;
   p.tile_begin = tile_begin;
   return p;
 }

@@ -32,9 +32,13 @@
 
 namespace flce {
 
-template <int kRows>
+// kSplit: epilogue warps per (lane quarter, 128-row half): 1 drains all 256 columns of its
+// rows, 2 gives each of two warps 128 of them (16 epilogue warps on wide tiles), which halves
+// the time a finished tile keeps the single accumulator of the wide geometry busy.
+template <int kRows, int kSplit = 1>
 struct PairGeom {
   static_assert(kRows == 128 || kRows == 256, "rows per CTA: 128 or 256");
+  static_assert(kSplit == 1 || kSplit == 2, "epilogue warps per row block: 1 or 2");
   static constexpr int kHalves = kRows / 128;          // M=256 MMAs per K step / epilogue halves
   static constexpr int kStages = kRows == 128 ? 6 : 4;
   static constexpr uint32_t kABytes = kRows * 128;     // kRows rows x 64 bf16
@@ -42,9 +46,10 @@ struct PairGeom {
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
   static constexpr int kAccBufs = 2 / kHalves;         // accumulators in the 512 TMEM columns
-  static constexpr int kEpiWarps = 4 * kHalves;
+  static constexpr int kEpiWarps = 4 * kHalves * kSplit;
   // ring, barrier/slot block (1 KB), store staging per epilogue warp, alignment slack
   static constexpr uint32_t kSmemBytes = kRingBytes + 1024 + kEpiWarps * kEpiStageBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr int kTileRows = 2 * kRows;          // M rows of one pair tile
 };
@@ -52,14 +57,14 @@ constexpr int kPairBK = 64;
 
 // GemmProblem::m_tiles counts pair tiles of 2 kRows rows (make_problem with tile_rows =
 // PairGeom<kRows>::kTileRows) and the epilogue receives 128-row block indices.
-template <int kRows, class Epi0, class Epi1>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kThreads, 1)
+template <int kRows, int kSplit, class Epi0, class Epi1>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSplit>::kThreads, 1)
     k_umma_gemm_pair(const __grid_constant__ CUtensorMap tA0,
                      const __grid_constant__ CUtensorMap tB0,
                      const __grid_constant__ CUtensorMap tA1,
                      const __grid_constant__ CUtensorMap tB1, const GemmGrid g,
                      const typename Epi0::Args e0, const typename Epi1::Args e1) {
-  using G = PairGeom<kRows>;
+  using G = PairGeom<kRows, kSplit>;
   constexpr int kPairStages = G::kStages;
   constexpr uint32_t kPairABytes = G::kABytes;
   constexpr uint32_t kPairStageBytes = G::kStageBytes;
@@ -69,8 +74,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPairRingBytes);
   // bars: [0,S) full, [S,2S) empty, [2S,2S+2) tmem_full, [2S+2,2S+4) tmem_empty, [2S+4] drain
-  // [2S+5, 2S+5+Q) tile-queue full, [2S+5+Q, 2S+5+2Q) tile-queue empty (used in the leader)
-  uint32_t* slots = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5 + 2 * kTileQueue);
+  // [2S+5, 2S+5+Q) tile-queue full, [2S+5+Q, 2S+5+2Q) tile-queue empty (used in the leader),
+  // [2S+5+2Q, 2S+5+2Q+8) epilogue exchange, one per (lane quarter, half) row block (split 2)
+  constexpr int kXBars = 8;
+  uint32_t* slots =
+      reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5 + 2 * kTileQueue + kXBars);
   uint32_t* tmem_slot = slots;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(slots + 1);
   int* issued_fills = reinterpret_cast<int*>(slots + 2);
@@ -90,6 +98,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
   auto drain_bar = [&]() { return bar0 + 8u * (2 * kPairStages + 4); };
   auto tq_full = [&](int q) { return bar0 + 8u * (2 * kPairStages + 5 + q); };
   auto tq_empty = [&](int q) { return bar0 + 8u * (2 * kPairStages + 5 + kTileQueue + q); };
+  auto x_bar = [&](int i) { return bar0 + 8u * (2 * kPairStages + 5 + 2 * kTileQueue + i); };
   // Tile indices flow through a small queue in each CTA: the leader's producer takes the next
   // tile (fixed stride or the shared counter) and writes it into both CTAs' queues; the
   // leader's MMA thread, the peer's producer and the epilogue warps of both CTAs read it and
@@ -115,6 +124,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
       mbar_init(tq_full(q), 1);
       mbar_init(tq_empty(q), 2 + 2 * G::kEpiWarps);
     }
+    for (int i = 0; i < kXBars; ++i) mbar_init(x_bar(i), 32);  // every lane of part 1
     *abort_flag = 0;
     *issued_fills = 0;
     *consumed_fills = 0;
@@ -282,11 +292,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue (both CTAs)
+    // Epilogue warp e = warp - 2 drains lane quarter warp % 4 (the quarter a warp may access)
+    // of 128-row half (e / 4) % kHalves, column part e / (4 kHalves) of kSplit.
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int grp = (warp - 2) >> 2;
+    const int half = grp % G::kHalves;
+    const int part = grp / G::kHalves;
     const int row = quarter * 32 + lane;
     uint4* stage = reinterpret_cast<uint4*>(smem + kPairRingBytes + 1024 +
                                             static_cast<uint32_t>(warp - 2) * kEpiStageBytes);
+    // the part-0 warp of this row block lends the exchange slots (epilogues that combine
+    // per-row partials across the two parts do not use store staging)
+    const int e_part0 = 4 * half + ((quarter - 2) & 3);
+    float2* xchg = reinterpret_cast<float2*>(smem + kPairRingBytes + 1024 +
+                                             static_cast<uint32_t>(e_part0) * kEpiStageBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     typename Epi0::State st0;
@@ -295,6 +314,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
     Epi1::init(e1, st1);
     int qslot = 0;
     uint32_t qphase = 0;
+    int iter = 0;
     while (true) {
       if (!mbar_wait_cluster(tq_full(qslot), qphase, g.status, abort_flag)) break;
       const int t = tile_q[qslot];
@@ -310,12 +330,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
       __syncwarp();
       const TileInfo pt = map_tile(g, t);
       const int mb128 = (pt.mb * 2 + static_cast<int>(rank)) * G::kHalves + half;
-      const uint32_t taddr = tmem_base + static_cast<uint32_t>((acc * G::kHalves + half) * kBN) +
-                             (static_cast<uint32_t>(quarter * 32) << 16);
+      EpiCtx ctx;
+      ctx.row = row;
+      ctx.taddr = tmem_base + static_cast<uint32_t>((acc * G::kHalves + half) * kBN) +
+                  (static_cast<uint32_t>(quarter * 32) << 16);
+      ctx.stage = stage;
+      ctx.c_begin = part * (kBN / 32 / kSplit);
+      ctx.c_end = ctx.c_begin + kBN / 32 / kSplit;
+      ctx.part = part;
+      ctx.split = kSplit;
+      ctx.iter = iter++;
+      ctx.two_acc = 0;
+      ctx.taddr_corr = 0;
+      ctx.xbar = x_bar(quarter + 4 * half);
+      ctx.xchg = xchg;
+      ctx.status = g.status;
+      ctx.abort = abort_flag;
       if (pt.prob == 0)
-        Epi0::tile(e0, st0, mb128, pt.nb, row, taddr, stage);
+        Epi0::tile(e0, st0, mb128, pt.nb, ctx);
       else
-        Epi1::tile(e1, st1, mb128, pt.nb, row, taddr, stage);
+        Epi1::tile(e1, st1, mb128, pt.nb, ctx);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
@@ -362,9 +396,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows>::kTh
 
 // How many CTA pairs of `kern` can be resident at once on the current device (queried once
 // per device and kernel). Depends on how the chip's SMs are grouped, not only on their count.
-template <int kRows, class K>
+template <int kRows, int kSplit, class K>
 int pair_resident_clusters(K kern, int sms) {
-  using G = PairGeom<kRows>;
+  using G = PairGeom<kRows, kSplit>;
   static int cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return sms / 2;
@@ -385,16 +419,16 @@ int pair_resident_clusters(K kern, int sms) {
 // Launch one or two problems on CTA pairs: a persistent grid of as many pairs as can be
 // resident at once (at most one per tile). The problems' m_tiles count PairGeom<kRows>::
 // kTileRows-row tiles, and K-major A operands are boxed {64 x kRows}.
-template <int kRows, class Epi0, class Epi1>
+template <int kRows, int kSplit, class Epi0, class Epi1>
 cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
                         const CUtensorMap& b1, GemmGrid g, const typename Epi0::Args& e0,
                         const typename Epi1::Args& e1, int sms, cudaStream_t stream) {
-  using G = PairGeom<kRows>;
-  auto kern = k_umma_gemm_pair<kRows, Epi0, Epi1>;
+  using G = PairGeom<kRows, kSplit>;
+  auto kern = k_umma_gemm_pair<kRows, kSplit, Epi0, Epi1>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int max_clusters = pair_resident_clusters<kRows>(kern, sms);
+  const int max_clusters = pair_resident_clusters<kRows, kSplit>(kern, sms);
   finish_grid(g);
   if (g.tile_counter) {
     e = cudaMemsetAsync(g.tile_counter, 0, sizeof(int), stream);
@@ -407,14 +441,20 @@ cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& b0, const CUte
 }
 
 // Launch on a pair core (kCorePair: 128-row CTA tiles, kCoreWide: 256-row CTA tiles); the
-// problems must have been made with core_tile_rows(core).
-template <class Epi0, class Epi1>
+// problems must have been made with core_tile_rows(core). kSplitWide: epilogue warps per row
+// block on the wide core (2 for roles whose epilogues fit the smaller register budget of 576
+// threads, when `role` is in the tune_split_epilogue() mask).
+template <class Epi0, class Epi1, int kSplitWide = 1>
 cudaError_t launch_pair_core(Core core, const CUtensorMap& a0, const CUtensorMap& b0,
                              const CUtensorMap& a1, const CUtensorMap& b1, GemmGrid g,
                              const typename Epi0::Args& e0, const typename Epi1::Args& e1, int sms,
-                             cudaStream_t stream) {
-  if (core == kCoreWide) return launch_pair<256, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
-  return launch_pair<128, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
+                             cudaStream_t stream, int role = 0) {
+  if (core == kCoreWide) {
+    if (kSplitWide == 2 && (tune_split_epilogue() & role) != 0)
+      return launch_pair<256, kSplitWide, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
+    return launch_pair<256, 1, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
+  }
+  return launch_pair<128, 1, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
 }
 
 }  // namespace flce

@@ -192,7 +192,9 @@ def test_tuning_knobs_validate(lib):
     assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_ROWS) == 2048
     for key, bad in [(B.FLCE_TUNE_RASTER_ROWS, 100), (B.FLCE_TUNE_RASTER_ROWS, 0),
                      (B.FLCE_TUNE_SM_PAIRS, 8), (B.FLCE_TUNE_SM_PAIRS, -2),
-                     (B.FLCE_TUNE_WIDE_TILES, 8), (B.FLCE_TUNE_WIDE_TILES, -2), (99, 1)]:
+                     (B.FLCE_TUNE_WIDE_TILES, 8), (B.FLCE_TUNE_WIDE_TILES, -2),
+                     (B.FLCE_TUNE_RASTER_VOCAB, 100), (B.FLCE_TUNE_RASTER_VOCAB, -256),
+                     (B.FLCE_TUNE_SPLIT_EPILOGUE, 8), (B.FLCE_TUNE_SPLIT_EPILOGUE, -2), (99, 1)]:
         with pytest.raises(B.FlceError):
             B.flce_set_tuning(key, bad)
     B.flce_set_tuning(B.FLCE_TUNE_RASTER_ROWS, 4096)
@@ -208,6 +210,21 @@ def test_tuning_knobs_validate(lib):
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
     assert B.flce_get_tuning(B.FLCE_TUNE_WIDE_TILES) == 7
+    # vocabulary raster groups: off by default, multiples of 256 when set
+    assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_VOCAB) == 0
+    B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 8192)
+    try:
+        assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_VOCAB) == 8192
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 0)
+    # two epilogue warps per row block: forward and dz by default; -1 restores the default
+    assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == B.FLCE_ROLE_FORWARD | B.FLCE_ROLE_DZ
+    B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, 0)
+    try:
+        assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == 0
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
+    assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == B.FLCE_ROLE_FORWARD | B.FLCE_ROLE_DZ
 
 
 def test_single_call_chunk_rule(lib):

@@ -161,16 +161,20 @@ def test_parity_single_sm_and_sm_pair_tiles(pair, wide):
 
 
 def test_contraction_cores_agree():
-    """The three contraction cores (single-SM, SM pairs with 128-row and with 256-row CTA tiles)
-    sum every output element over K in the same order, so all outputs agree bit for bit, for
-    both schedules."""
+    """The three contraction cores (single-SM, SM pairs with 128-row and with 256-row CTA tiles,
+    the last with one or two epilogue warps per row block, and in either raster order) sum
+    every output element over K in the same order and form every per-row partial the same
+    way, so all outputs agree bit for bit, for both schedules."""
     inp = make_inputs("tiny", T=1100, H=320, V=3000, dtype="bf16", seed=33)
     x, w, y = to_device(inp)
     outs, fused = [], []
     try:
-        for pair, wide in [(0, 0), (7, 0), (7, 7)]:
+        for pair, wide, split, rv in [(0, 0, -1, 0), (7, 0, -1, 0), (7, 7, -1, 0), (7, 7, 0, 0),
+                                      (7, 7, -1, 1024)]:
             B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
             B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
+            B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, split)
+            B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, rv)
             loss, lse, status = A.flce_forward(x, w, y, "mean")
             gx, gw, status_b = A.flce_backward(x, w, y, lse, torch.ones((), device="cuda"), "mean")
             torch.cuda.synchronize()
@@ -182,6 +186,8 @@ def test_contraction_cores_agree():
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
+        B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
+        B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 0)
     for other in outs[1:]:
         for a, b in zip(outs[0], other):
             assert np.array_equal(a, b)
