@@ -136,10 +136,13 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
  * fused_linear_cross_entropy kernel" (Helion PR #1268) computes the gradients inside the forward
  * over token chunks; "feat(FLCE): add helion version of fused linear cross entropy"
  * (Liger-Kernel PR #928) reports its chunk-materialised backward as sound. Here the logits of a
- * chunk of tokens (at most half of all tokens and at most 2 GiB of bf16) are computed once and
- * turned into dz in place, so the call does 6 T H V FLOPs instead of the 8 T H V of
- * flce_forward + flce_backward, at the price of the chunk buffer and an fp32 grad_weight
- * accumulator in the workspace.
+ * chunk of tokens (at most half of all tokens and at most FLCE_TUNE_CHUNK_BYTES of bf16, 1.5 GiB
+ * by default) are computed once and turned into dz in place, so the call does 6 T H V FLOPs
+ * instead of the 8 T H V of flce_forward + flce_backward, at the price of the chunk buffer in
+ * the workspace. grad_weight is summed over the chunks in its own output: the first chunk writes
+ * it and each later chunk adds its part in fp32 and rounds the sum back to bf16, so for n chunks
+ * it is rounded n times (a relative error of at most about n 2^-9 of the largest partial sums,
+ * against 2^-9 for flce_backward, whose grad_weight is rounded once).
  *   Arguments as for flce_forward and flce_backward together: grad_loss (device, [1] or [T] for
  *   FLCE_REDUCTION_NONE) is read by the call; loss, lse, grad_x and grad_weight are written.
  *   bf16 with T >= 512 uses the chunked schedule; otherwise the call runs flce_forward followed
@@ -228,13 +231,20 @@ int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_RO
  *                          released sooner, at the price of fewer registers per thread. A bit mask
  *                          of FLCE_ROLE_FORWARD (forward projection and single-call chunk
  *                          logits) and FLCE_ROLE_DZ; FLCE_ROLE_GRADS is ignored. -1 restores
- *                          the default (FLCE_ROLE_FORWARD | FLCE_ROLE_DZ).
+ *                          the default, 0 (measured no faster on GB300).
+ *   FLCE_TUNE_CHUNK_BYTES  bytes of bf16 chunk logits the single call (flce_forward_backward)
+ *                          may hold at once: it takes as few token chunks of (nearly) equal size
+ *                          as this budget and the half-of-all-tokens limit allow. Fewer chunks
+ *                          mean fewer passes over grad_weight, more chunks less memory. 0
+ *                          restores the default, 1.5 GiB. Affects the size query and the call
+ *                          alike, so set it before querying the workspace size.
  * Read at each launch. Returns FLCE_OK or FLCE_ERR_ARG. */
 #define FLCE_TUNE_RASTER_ROWS 1
 #define FLCE_TUNE_SM_PAIRS 2
 #define FLCE_TUNE_WIDE_TILES 3
 #define FLCE_TUNE_RASTER_VOCAB 4
 #define FLCE_TUNE_SPLIT_EPILOGUE 5
+#define FLCE_TUNE_CHUNK_BYTES 6
 #define FLCE_ROLE_FORWARD 1
 #define FLCE_ROLE_DZ 2
 #define FLCE_ROLE_GRADS 4

@@ -463,6 +463,8 @@ struct GradWEpi {
 //   mode 1: first slab  -> acc = D
 //   mode 2: middle slab -> acc += D
 //   mode 3: last slab   -> out = acc + D
+//   mode 4: out += D, read and rounded back in the output type (bf16 outputs only): the
+//           single call's grad_weight summed over token chunks in its own output buffer
 // For fp32 outputs `acc` and `out` are the same buffer.
 // As for grad_W, the slab product is scaled by g in fp32 before it is accumulated.
 template <bool kF32Out>
@@ -515,7 +517,7 @@ struct GradXEpi {
           transpose_rows64(stage, in, out[hh], lane);
         }
         float4 p[2][4];
-        if (a.mode >= 2) {
+        if (a.mode == 2 || a.mode == 3) {
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
@@ -525,6 +527,20 @@ struct GradXEpi {
               p[hh][q] = (tr < a.T && col < a.H)
                              ? *reinterpret_cast<const float4*>(a.acc + static_cast<size_t>(tr) * a.H + col)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        } else if (a.mode == 4) {
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int tr = t0 + 8 * q + qa;
+              const int col = h0 + 16 * hh + 4 * qb;
+              uint2 u = make_uint2(0u, 0u);
+              if (tr < a.T && col < a.H)
+                u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(a.out) +
+                                                    static_cast<size_t>(tr) * a.H + col);
+              p[hh][q] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
             }
         }
 #pragma unroll

@@ -280,11 +280,13 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // ---- single-call forward + backward (token chunks, no logits recompute)
 
-// bf16 chunk logits per chunk. Larger chunks mean fewer fp32 read-modify-write passes over the
-// grad_weight accumulator (one per chunk): 2 GiB halves them against 1 GiB at V = 128256
-// (measured: the single call's gradient launches 20.3 -> 18.5 ms per step at T = 16384).
-constexpr int64_t kChunkBudgetBytes = int64_t(1) << 31;
+// bf16 chunk logits per chunk (FLCE_TUNE_CHUNK_BYTES). grad_weight is summed over the chunks in
+// its own bf16 output (the first chunk writes it, every later one reads, adds and rounds it
+// back), so the workspace holds no V x H accumulator and a chunk count n moves (2n - 1) V H 2
+// bytes of grad_weight; 1.5 GiB gives 3 chunks at T = 16384, V = 128256 (workspace 1.46 GB,
+// below the 4.2 GB of bf16 logits with x, weight and both gradients included).
 constexpr int64_t kMinFusedTokens = 512;
+std::atomic<int64_t> g_chunk_bytes{flce::kDefaultChunkBytes};
 
 // The chunked single-call schedule applies to bf16 with at least 512 tokens (so a chunk never
 // holds all tokens' logits); otherwise flce_forward_backward runs flce_forward + flce_backward.
@@ -294,7 +296,7 @@ bool fused_schedule(int64_t T, int dtype) {
 
 int64_t fused_chunk_rows(int64_t T, int64_t V) {
   const int64_t ldz = round_up(V, kTileN);
-  int64_t c = kChunkBudgetBytes / (2 * ldz) / 256 * 256;
+  int64_t c = g_chunk_bytes.load() / (2 * ldz) / 256 * 256;
   const int64_t half = round_up(cdiv(T, 2), 256);
   if (c > half) c = half;
   if (c < 256) c = 256;
@@ -305,7 +307,7 @@ int64_t fused_chunk_rows(int64_t T, int64_t V) {
 struct FusedWs {
   int64_t rows, ldz, n_chunks;
   __nv_bfloat16* zbuf;
-  float *part_m, *part_s, *zy, *block_sums, *gw_acc;
+  float *part_m, *part_s, *zy, *block_sums;
   int* counter;
 };
 
@@ -320,7 +322,6 @@ size_t carve_fused(Carver& c, int64_t T, int64_t H, int64_t V, FusedWs* w) {
   r.part_s = static_cast<float*>(c.take(sizeof(float) * nt * r.rows));
   r.zy = static_cast<float*>(c.take(sizeof(float) * r.rows));
   r.block_sums = static_cast<float*>(c.take(sizeof(float) * cdiv(T, 256)));
-  if (r.n_chunks > 1) r.gw_acc = static_cast<float*>(c.take(sizeof(float) * V * H));
   r.counter = static_cast<int*>(c.take(sizeof(int)));
   if (w) *w = r;
   return c.off;
@@ -441,6 +442,10 @@ int flce_set_tuning(int key, int64_t value) {
       if (value < 0 || value > (int64_t(1) << 24) || value % 256 != 0) return FLCE_ERR_ARG;
       flce::g_tune_raster_vocab.store(static_cast<int>(value));
       return FLCE_OK;
+    case FLCE_TUNE_CHUNK_BYTES:
+      if (value < 0 || value > (int64_t(1) << 40)) return FLCE_ERR_ARG;
+      g_chunk_bytes.store(value == 0 ? flce::kDefaultChunkBytes : value);
+      return FLCE_OK;
     case FLCE_TUNE_SPLIT_EPILOGUE:
       if (value < -1 || value > 7) return FLCE_ERR_ARG;
       flce::g_tune_split_epilogue.store(value < 0 ? flce::kDefaultSplitEpilogue
@@ -466,6 +471,9 @@ int flce_get_tuning(int key, int64_t* value) {
       return FLCE_OK;
     case FLCE_TUNE_SPLIT_EPILOGUE:
       *value = flce::g_tune_split_epilogue.load();
+      return FLCE_OK;
+    case FLCE_TUNE_CHUNK_BYTES:
+      *value = g_chunk_bytes.load();
       return FLCE_OK;
     case FLCE_TUNE_SM_PAIRS: {
       flce::Device dev;
@@ -801,8 +809,7 @@ int flce_forward_backward(const void* x, const void* weight, const int64_t* targ
     cl.zy = w.zy;
     cl.grad_x_rows = static_cast<uint8_t*>(grad_x) + size_t(t0) * H * 2;
     cl.grad_w = grad_weight;
-    cl.gw_acc = w.gw_acc;
-    cl.gw_mode = w.n_chunks == 1 ? 0 : (ci == 0 ? 1 : (ci == w.n_chunks - 1 ? 3 : 2));
+    cl.gw_mode = ci == 0 ? 0 : 4;  // written by the first chunk, summed in place after it
     cl.tile_counter = w.counter;
     cl.rows = int(rows);
     cl.H = int(H);

@@ -10,8 +10,9 @@
 //                half-tile) plus lse partials per half-tile (LogitsEpi)
 //   2. combine : lse, per-token loss / loss block sums of the chunk rows (k_fwd_combine)
 //   3. form dz : dz = (exp(z - lse) - onehot) * row scale, in place, bf16 (k_form_dz)
-//   4. grads   : grad_x[chunk] = dz . W (complete, K = V) and grad_W (+)= dz^T . x_c (K = Tc,
-//                fp32 accumulation over chunks in chunk order), one launch, dynamic tiles
+//   4. grads   : grad_x[chunk] = dz . W (complete, K = V) and grad_W (+)= dz^T . x_c (K = Tc),
+//                one launch, dynamic tiles; grad_W is written by the first chunk and summed in
+//                place, in its bf16 output, by the later ones (in chunk order)
 // FLOPs: 6 T H V (forward + two gradient contractions) instead of 8 T H V with recompute.
 #include "epilogues.cuh"
 #include "flce_internal.h"
@@ -90,8 +91,8 @@ cudaError_t launch_chunk_grads(const CUtensorMap& tz_k, const CUtensorMap& tw_mn
                                const ChunkLaunch& c) {
   typename GradXEpi<false>::Args ex{nullptr, c.grad_x_rows, c.grad_loss, c.scale,
                                     c.rows,  c.H,           0};
-  typename GradXEpi<false>::Args ew{c.gw_acc, c.grad_w, c.grad_loss, c.scale,
-                                    c.V,      c.H,      c.gw_mode};
+  typename GradXEpi<false>::Args ew{nullptr, c.grad_w, c.grad_loss, c.scale,
+                                    c.V,     c.H,      c.gw_mode};
   const Core core = role_core(c.sms, FLCE_ROLE_GRADS);  // zbuf K-major map boxed to match
   const int tile_rows = core_tile_rows(core);
   GemmGrid g{};

@@ -47,8 +47,13 @@ constexpr int kAutoPairRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ | FLCE_ROLE_GRAD
 // launch.
 constexpr int kDefaultRasterVocab = 0;
 
-// Default of tune_split_epilogue().
-constexpr int kDefaultSplitEpilogue = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ;
+// Default bf16 chunk-logits budget of the single call (FLCE_TUNE_CHUNK_BYTES): 1.5 GiB.
+constexpr int64_t kDefaultChunkBytes = int64_t(3) << 29;
+
+// Default of tune_split_epilogue(): none. Measured on GB300 at the headline size and on the
+// Llama-2 head: two epilogue warps per row block left the tensor pipe's active cycles where
+// they were (dz 85.8% -> 85.2%, forward 89.3% -> 89.4%) and the launches 0.3% slower.
+constexpr int kDefaultSplitEpilogue = 0;
 
 // Roles measured faster on 256-row CTA tiles when they run on CTA pairs.
 constexpr int kDefaultWideRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ | FLCE_ROLE_GRADS;
@@ -186,8 +191,7 @@ struct ChunkLaunch {
   float *part_m, *part_s, *zy;  // [ldz / 128][rows] (one per half-tile) x 2, [rows]
   void* grad_x_rows;       // grad_x + t0 * H
   void* grad_w;
-  float* gw_acc;           // fp32 [V][H] accumulator across chunks
-  int gw_mode;             // 0 only chunk, 1 first, 2 middle, 3 last
+  int gw_mode;             // 0: the first chunk writes grad_w, 4: later chunks add to it
   int* tile_counter;
   int rows, H, V;
   int* status;

@@ -194,7 +194,8 @@ def test_tuning_knobs_validate(lib):
                      (B.FLCE_TUNE_SM_PAIRS, 8), (B.FLCE_TUNE_SM_PAIRS, -2),
                      (B.FLCE_TUNE_WIDE_TILES, 8), (B.FLCE_TUNE_WIDE_TILES, -2),
                      (B.FLCE_TUNE_RASTER_VOCAB, 100), (B.FLCE_TUNE_RASTER_VOCAB, -256),
-                     (B.FLCE_TUNE_SPLIT_EPILOGUE, 8), (B.FLCE_TUNE_SPLIT_EPILOGUE, -2), (99, 1)]:
+                     (B.FLCE_TUNE_SPLIT_EPILOGUE, 8), (B.FLCE_TUNE_SPLIT_EPILOGUE, -2),
+                     (B.FLCE_TUNE_CHUNK_BYTES, -1), (99, 1)]:
         with pytest.raises(B.FlceError):
             B.flce_set_tuning(key, bad)
     B.flce_set_tuning(B.FLCE_TUNE_RASTER_ROWS, 4096)
@@ -217,34 +218,48 @@ def test_tuning_knobs_validate(lib):
         assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_VOCAB) == 8192
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 0)
-    # two epilogue warps per row block: forward and dz by default; -1 restores the default
-    assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == B.FLCE_ROLE_FORWARD | B.FLCE_ROLE_DZ
-    B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, 0)
+    # two epilogue warps per row block: off by default; -1 restores the default
+    assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == 0
+    B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, B.FLCE_ROLE_FORWARD | B.FLCE_ROLE_DZ)
     try:
-        assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == 0
+        assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == 3
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
-    assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == B.FLCE_ROLE_FORWARD | B.FLCE_ROLE_DZ
+    assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == 0
 
 
 def test_single_call_chunk_rule(lib):
     """Tokens per chunk of the single-call schedule: a multiple of 256, at most half of T (so no
-    chunk ever holds all tokens' logits) and at most 2 GiB of bf16 logits; bf16 only, T >= 512."""
+    chunk ever holds all tokens' logits) and at most FLCE_TUNE_CHUNK_BYTES (1.5 GiB by default)
+    of bf16 logits; bf16 only, T >= 512. The workspace holds the chunk buffer and the per-half-
+    tile partials, no V x H accumulator, so at the headline size the whole call (inputs and
+    gradients included) stays below the bf16 logits it avoids."""
     bf16 = B.FLCE_DTYPE_BF16
-    assert B.flce_forward_backward_chunk_tokens(16384, 4096, 128256, bf16) == 8192
-    assert B.flce_forward_backward_chunk_tokens(32768, 4096, 128256, bf16) == 8192
+    assert B.flce_get_tuning(B.FLCE_TUNE_CHUNK_BYTES) == 3 << 29
+    assert B.flce_forward_backward_chunk_tokens(16384, 4096, 128256, bf16) == 5632  # 3 chunks
+    assert B.flce_forward_backward_chunk_tokens(32768, 4096, 128256, bf16) == 5632  # 6 chunks
     assert B.flce_forward_backward_chunk_tokens(4096, 4096, 32000, bf16) == 2048
     assert B.flce_forward_backward_chunk_tokens(1269, 1000, 10000, bf16) == 768
     assert B.flce_forward_backward_chunk_tokens(300, 256, 1500, bf16) == 300  # below 512: T
     assert B.flce_forward_backward_chunk_tokens(16384, 4096, 128256, B.FLCE_DTYPE_F32) == 16384
     # Gemma-3-sized head: 3 chunks of nearly equal size (2816 + 2816 + 2560), not 3840 + 3840 + 512
     assert B.flce_forward_backward_chunk_tokens(8192, 2304, 262208, bf16) == 2816
+    T, H, V = 16384, 4096, 128256
+    ws = B.flce_forward_backward_workspace_size(T, H, V, bf16)
+    assert ws + 2 * 2 * H * (T + V) < 2 * T * V  # x, weight, grad_x, grad_weight + workspace
     for T, V in [(16384, 128256), (32768, 151936), (8192, 262208), (600, 513), (100000, 50000)]:
         c = B.flce_forward_backward_chunk_tokens(T, 4096, V, bf16)
         ldz = -(-V // 256) * 256
         assert c % 256 == 0 and c >= 256
         assert c <= -(-T // 2 // 256) * 256 + 256 and c < T
-        assert c == 256 or 2 * c * ldz <= 1 << 31
+        assert c == 256 or 2 * c * ldz <= 3 << 29
+    # the budget is a knob: 2 GiB gives 2 chunks of 8192 at the headline size; 0 restores it
+    B.flce_set_tuning(B.FLCE_TUNE_CHUNK_BYTES, 1 << 31)
+    try:
+        assert B.flce_forward_backward_chunk_tokens(16384, 4096, 128256, bf16) == 8192
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_CHUNK_BYTES, 0)
+    assert B.flce_forward_backward_chunk_tokens(16384, 4096, 128256, bf16) == 5632
 
 
 def _fb(**kw):
@@ -337,11 +352,11 @@ def test_plain_c_caller(lib, tmp_path):
 
 def test_sizing_rules_hold_on_random_shapes(lib):
     """The slab, chunk and workspace sizes for 300 random shapes (log-uniform T and V, both
-    dtypes): 256-column granularity, no empty slab or chunk, the 1 GiB slab and 2 GiB chunk
+    dtypes): 256-column granularity, no empty slab or chunk, the 1 GiB slab and 1.5 GiB chunk
     budgets, as few slabs as the budget allows, slabs and chunks of nearly equal size, and
     workspaces that hold what the kernels write (for bf16, nothing more than that)."""
     r = np.random.default_rng(2024)
-    budget_slab, budget_chunk = 1 << 30, 1 << 31
+    budget_slab, budget_chunk = 1 << 30, 3 << 29
     up = lambda a, b: -(-a // b) * b  # noqa: E731
     for _ in range(300):
         T = int(np.exp(r.uniform(0, np.log(1 << 18))))
@@ -379,7 +394,8 @@ def test_sizing_rules_hold_on_random_shapes(lib):
             assert c == 256 or 2 * c * ldz <= budget_chunk, label
             assert c - (T - (k - 1) * c) <= 256 * k, label
             fbs = B.flce_forward_backward_workspace_size(T, H, V, dt)
-            assert fbs >= 2 * c * ldz + (4 * V * H if k > 1 else 0), label
+            need = 2 * c * ldz + 2 * 4 * (ldz // 128) * c  # chunk logits + half-tile partials
+            assert need <= fbs <= need + 4 * c + 4 * (T // 256 + 1) + 4096, label
 
 
 def test_missing_library_fails_loudly(lib, monkeypatch, tmp_path):
