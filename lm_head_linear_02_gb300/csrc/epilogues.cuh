@@ -122,10 +122,11 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
 struct FwdEpi {
   struct Args {
     const int64_t* target;
-    float* part_m;  // [n_tiles][T]
+    float* part_m;  // [n_tiles][T], n_tiles = ceil(V_total / 256)
     float* part_s;  // [n_tiles][T]
     float* zy;      // [T]
-    int T, V;
+    int T, V;       // V: vocab columns of this launch
+    int col0;       // vocab column of the launch's first column (a multiple of 256)
   };
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
@@ -185,8 +186,8 @@ struct FwdEpi {
                                               const EpiCtx& ctx) {
     const int t = mb * kBM + ctx.row;
     const bool valid = t < a.T;
-    const int n0 = nb * kBN;
-    const long long y = valid ? static_cast<long long>(a.target[t]) : -1ll;
+    const int n0 = nb * kBN;  // launch-relative column of the tile
+    const long long y = valid ? static_cast<long long>(a.target[t]) - a.col0 : -1ll;
     const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
     constexpr int kHalfChunks = kBN / 64;
     float zy = 0.f;
@@ -211,7 +212,7 @@ struct FwdEpi {
       }
     }
     if (valid && ctx.part == 0) {
-      const size_t o = static_cast<size_t>(nb) * a.T + t;
+      const size_t o = static_cast<size_t>(a.col0 / kBN + nb) * a.T + t;
       a.part_m[o] = m;
       a.part_s[o] = s;
     }

@@ -192,8 +192,21 @@ struct Carver {
 struct FwdWs {
   float *part_m, *part_s, *zy, *block_sums;
   int* counter;                      // tile counter of the projection launch
-  float *x_hi, *x_lo, *w_hi, *w_lo;  // f32 path only
+  float *x_hi, *x_lo, *w_hi, *w_lo;  // f32 path only: x [T][H]; one weight slab [vf][H]
+  int64_t vf;                        // f32 path: weight rows per projection launch
 };
+
+// fp32 path: weight rows whose TF32 hi/lo copies the forward holds at once (the projection runs
+// slab by slab): at most 256 MB of copies, a multiple of 256, slabs of nearly equal width.
+constexpr int64_t kFwdSlabBytesF32 = int64_t(1) << 28;
+
+int64_t fwd_slab_width_f32(int64_t H, int64_t V) {
+  const int64_t vmax = round_up(V, kTileN);
+  int64_t vf = kFwdSlabBytesF32 / (8 * H) / kTileN * kTileN;
+  if (vf < kTileN) vf = kTileN;
+  if (vf >= vmax) return vmax;
+  return round_up(cdiv(V, cdiv(V, vf)), kTileN);
+}
 
 size_t carve_fwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, FwdWs* w) {
   const int64_t nt = cdiv(V, kTileN);
@@ -204,10 +217,11 @@ size_t carve_fwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, FwdWs* w
   r.block_sums = static_cast<float*>(c.take(sizeof(float) * cdiv(T, 256)));
   r.counter = static_cast<int*>(c.take(sizeof(int)));
   if (dtype == FLCE_DTYPE_F32) {
+    r.vf = fwd_slab_width_f32(H, V);
     r.x_hi = static_cast<float*>(c.take(sizeof(float) * T * H));
     r.x_lo = static_cast<float*>(c.take(sizeof(float) * T * H));
-    r.w_hi = static_cast<float*>(c.take(sizeof(float) * V * H));
-    r.w_lo = static_cast<float*>(c.take(sizeof(float) * V * H));
+    r.w_hi = static_cast<float*>(c.take(sizeof(float) * r.vf * H));
+    r.w_lo = static_cast<float*>(c.take(sizeof(float) * r.vf * H));
   }
   if (w) *w = r;
   return c.off;
@@ -215,12 +229,13 @@ size_t carve_fwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, FwdWs* w
 
 std::atomic<int64_t> g_slab_override{0};
 
-int64_t slab_width(int64_t T, int64_t V, int dtype) {
+int64_t slab_width(int64_t T, int64_t H, int64_t V, int dtype) {
   const int64_t vmax = round_up(V, kTileN);
   const int64_t forced = g_slab_override.load();
   if (forced > 0) return forced < vmax ? forced : vmax;
-  // bf16: one bf16 slab. f32: hi/lo slabs in both [T][Vc] and [Vc][T] orientation.
-  const int64_t per_col = dtype == FLCE_DTYPE_BF16 ? 2 * T : 16 * round_up(T, 4);
+  // bf16: one bf16 slab. f32: dz hi/lo slabs in both [T][Vc] and [Vc][T] orientation, and the
+  // weight slab's hi/lo copies in both [Vc][H] and [H][Vc] orientation.
+  const int64_t per_col = dtype == FLCE_DTYPE_BF16 ? 2 * T : 16 * round_up(T, 4) + 16 * H;
   int64_t vc = kSlabBudgetBytes / per_col / kTileN * kTileN;
   if (vc < kTileN) vc = kTileN;
   if (vc >= vmax) return vmax;
@@ -229,23 +244,23 @@ int64_t slab_width(int64_t T, int64_t V, int dtype) {
 }
 
 struct BwdWs {
-  int64_t vc, n_slabs, ldT, ldV;
+  int64_t vc, n_slabs, ldT, ldVc;
   void* dz;       // bf16 [T][vc] or f32 hi [T][vc]
   float* dz_lo;   // [T][vc]
   float* dzt_hi;  // [vc][ldT]
   float* dzt_lo;
   float* acc;     // bf16 path, [T][H] when more than one slab
   float *x_hi, *x_lo, *xt_hi, *xt_lo;  // [T][H], [H][ldT]
-  float *w_hi, *w_lo, *wt_hi, *wt_lo;  // [V][H], [H][ldV]
+  float *w_hi, *w_lo, *wt_hi, *wt_lo;  // one weight slab: [vc][H], [H][ldVc]
   int* counter;                        // tile counter of the dz and gradient launches
 };
 
 size_t carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, BwdWs* w) {
   BwdWs r{};
-  r.vc = slab_width(T, V, dtype);
+  r.vc = slab_width(T, H, V, dtype);
   r.n_slabs = cdiv(V, r.vc);
   r.ldT = round_up(T, 4);
-  r.ldV = round_up(V, 4);
+  r.ldVc = round_up(r.vc, 4);
   if (dtype == FLCE_DTYPE_BF16) {
     r.dz = c.take(size_t(2) * T * r.vc);
     if (r.n_slabs > 1) r.acc = static_cast<float*>(c.take(sizeof(float) * T * H));
@@ -258,10 +273,10 @@ size_t carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, BwdWs* w
     r.x_lo = static_cast<float*>(c.take(sizeof(float) * T * H));
     r.xt_hi = static_cast<float*>(c.take(sizeof(float) * H * r.ldT));
     r.xt_lo = static_cast<float*>(c.take(sizeof(float) * H * r.ldT));
-    r.w_hi = static_cast<float*>(c.take(sizeof(float) * V * H));
-    r.w_lo = static_cast<float*>(c.take(sizeof(float) * V * H));
-    r.wt_hi = static_cast<float*>(c.take(sizeof(float) * H * r.ldV));
-    r.wt_lo = static_cast<float*>(c.take(sizeof(float) * H * r.ldV));
+    r.w_hi = static_cast<float*>(c.take(sizeof(float) * r.vc * H));
+    r.w_lo = static_cast<float*>(c.take(sizeof(float) * r.vc * H));
+    r.wt_hi = static_cast<float*>(c.take(sizeof(float) * H * r.ldVc));
+    r.wt_lo = static_cast<float*>(c.take(sizeof(float) * H * r.ldVc));
   }
   r.counter = static_cast<int*>(c.take(sizeof(int)));
   if (w) *w = r;
@@ -382,7 +397,7 @@ int64_t flce_forward_backward_chunk_tokens(int64_t T, int64_t H, int64_t V, int 
 
 int64_t flce_backward_slab_width(int64_t T, int64_t H, int64_t V, int dtype) {
   if (!dims_ok(T, H, V, dtype)) return 0;
-  return slab_width(T, V, dtype);
+  return slab_width(T, H, V, dtype);
 }
 
 int flce_test_withhold_signal(void) {
@@ -561,19 +576,27 @@ int flce_forward(const void* x, const void* weight, const int64_t* target, int64
       return FLCE_ERR_CUDA;
     e = flce::timed_launch(0, s, [&] { return flce::launch_forward_bf16(tx, tw, p); });
   } else {
-    CUtensorMap txh, txl, twh, twl;
+    // x split once; the weight split and projected slab by slab (w.vf rows at a time)
+    CUtensorMap txh, txl;
     const auto F = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     if (!flce::make_tmap_2d(&txh, F, w.x_hi, H, T, H * 4, 32, kTileM) ||
-        !flce::make_tmap_2d(&txl, F, w.x_lo, H, T, H * 4, 32, kTileM) ||
-        !flce::make_tmap_2d(&twh, F, w.w_hi, H, V, H * 4, 32, kTileN) ||
-        !flce::make_tmap_2d(&twl, F, w.w_lo, H, V, H * 4, 32, kTileN))
+        !flce::make_tmap_2d(&txl, F, w.x_lo, H, T, H * 4, 32, kTileM))
       return FLCE_ERR_CUDA;
     e = flce::launch_split_tf32(static_cast<const float*>(x), T, H, H, w.x_hi, w.x_lo, false, s);
-    if (e == cudaSuccess)
-      e = flce::launch_split_tf32(static_cast<const float*>(weight), V, H, H, w.w_hi, w.w_lo,
-                                  false, s);
-    if (e == cudaSuccess)
-      e = flce::timed_launch(0, s, [&] { return flce::launch_forward_tf32(txh, twh, txl, twl, p); });
+    for (int64_t v0 = 0; v0 < V && e == cudaSuccess; v0 += w.vf) {
+      const int64_t sw = (V - v0) < w.vf ? (V - v0) : w.vf;
+      CUtensorMap twh, twl;
+      if (!flce::make_tmap_2d(&twh, F, w.w_hi, H, sw, H * 4, 32, kTileN) ||
+          !flce::make_tmap_2d(&twl, F, w.w_lo, H, sw, H * 4, 32, kTileN))
+        return FLCE_ERR_CUDA;
+      e = flce::launch_split_tf32(static_cast<const float*>(weight) + size_t(v0) * H, sw, H, H,
+                                  w.w_hi, w.w_lo, false, s);
+      if (e == cudaSuccess)
+        e = flce::timed_launch(0, s, [&] {
+          return flce::launch_forward_tf32(txh, twh, txl, twl, p, int(v0), int(sw));
+        });
+    }
+    if (e == cudaSuccess) e = flce::launch_forward_combine(p);
   }
   return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
 }
@@ -636,11 +659,8 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
         !flce::make_tmap_2d(&txtl, DT, w.xt_lo, T, H, w.ldT * 4, bk, kTileN))
       return FLCE_ERR_CUDA;
     const float* xf = static_cast<const float*>(x);
-    const float* wf = static_cast<const float*>(weight);
     e = flce::launch_split_tf32(xf, T, H, H, w.x_hi, w.x_lo, false, s);
     if (e == cudaSuccess) e = flce::launch_split_tf32(xf, T, H, w.ldT, w.xt_hi, w.xt_lo, true, s);
-    if (e == cudaSuccess) e = flce::launch_split_tf32(wf, V, H, H, w.w_hi, w.w_lo, false, s);
-    if (e == cudaSuccess) e = flce::launch_split_tf32(wf, V, H, w.ldV, w.wt_hi, w.wt_lo, true, s);
     if (e != cudaSuccess) return FLCE_ERR_CUDA;
   }
 
@@ -709,15 +729,21 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
         e = flce::timed_launch(
             4, s, [&] { return flce::launch_grads_bf16(tdz_mn, tx_mn, tdz_k, tw_mn, gw, gx); });
     } else {
+      // this slab's weight rows split into TF32 hi/lo, as rows [sw][H] and transposed [H][sw]
+      const float* wslab = static_cast<const float*>(weight) + size_t(slab0) * H;
+      e = flce::launch_split_tf32(wslab, sw, H, H, w.w_hi, w.w_lo, false, s);
+      if (e == cudaSuccess)
+        e = flce::launch_split_tf32(wslab, sw, H, w.ldVc, w.wt_hi, w.wt_lo, true, s);
+      if (e != cudaSuccess) break;
       CUtensorMap twh, twl, tdzth, tdztl, tdzh, tdzl, twth, twtl;
-      if (!flce::make_tmap_2d(&twh, DT, w.w_hi + size_t(slab0) * H, H, sw, H * 4, bk, kTileN) ||
-          !flce::make_tmap_2d(&twl, DT, w.w_lo + size_t(slab0) * H, H, sw, H * 4, bk, kTileN) ||
+      if (!flce::make_tmap_2d(&twh, DT, w.w_hi, H, sw, H * 4, bk, kTileN) ||
+          !flce::make_tmap_2d(&twl, DT, w.w_lo, H, sw, H * 4, bk, kTileN) ||
           !flce::make_tmap_2d(&tdzth, DT, w.dzt_hi, T, sw, w.ldT * 4, bk, kTileM) ||
           !flce::make_tmap_2d(&tdztl, DT, w.dzt_lo, T, sw, w.ldT * 4, bk, kTileM) ||
           !flce::make_tmap_2d(&tdzh, DT, w.dz, sw, T, w.vc * 4, bk, kTileM) ||
           !flce::make_tmap_2d(&tdzl, DT, w.dz_lo, sw, T, w.vc * 4, bk, kTileM) ||
-          !flce::make_tmap_2d(&twth, DT, w.wt_hi + slab0, sw, H, w.ldV * 4, bk, kTileN) ||
-          !flce::make_tmap_2d(&twtl, DT, w.wt_lo + slab0, sw, H, w.ldV * 4, bk, kTileN))
+          !flce::make_tmap_2d(&twth, DT, w.wt_hi, sw, H, w.ldVc * 4, bk, kTileN) ||
+          !flce::make_tmap_2d(&twtl, DT, w.wt_lo, sw, H, w.ldVc * 4, bk, kTileN))
         return FLCE_ERR_CUDA;
       e = flce::timed_launch(1, s, [&] { return flce::launch_dz_tf32(txh, twh, txl, twl, dz); });
       if (e == cudaSuccess)

@@ -75,28 +75,24 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-static cudaError_t launch_combine(const FwdLaunch& p);
-
-// Projection + online log-sum-exp over all (token tile, vocab tile) pairs, then the combine
-// and finalize kernels.
+// Projection + online log-sum-exp over the (token tile, vocab tile) pairs of vocab columns
+// [col0, col0 + cols) (W maps cover those rows only).
 template <bool kTF32>
-static cudaError_t launch_forward(const CUtensorMap& tx, const CUtensorMap& tw,
-                                  const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
-                                  const FwdLaunch& p) {
+static cudaError_t launch_projection(const CUtensorMap& tx, const CUtensorMap& tw,
+                                     const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
+                                     const FwdLaunch& p, int col0, int cols) {
   GemmGrid g{};
-  g.p[0] = make_problem(p.T, p.V, p.H, StageGeom<kTF32>::kBK, false, false, kBM, 0, true);
+  g.p[0] = make_problem(p.T, cols, p.H, StageGeom<kTF32>::kBK, false, false, kBM, 0, true);
   g.num_problems = 1;
   g.status = p.status;
   g.tile_counter = p.tile_counter;
-  FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V};
-  cudaError_t e = launch_gemm<kTF32, FwdEpi, NoEpi>(tx, tw, tx_lo, tw_lo, g, ea, NoEpi::Args{},
-                                                    p.sms, p.stream);
-  if (e != cudaSuccess) return e;
-  return launch_combine(p);
+  FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, cols, col0};
+  return launch_gemm<kTF32, FwdEpi, NoEpi>(tx, tw, tx_lo, tw_lo, g, ea, NoEpi::Args{}, p.sms,
+                                           p.stream);
 }
 
 // The combine (lse, per-token loss, block sums) and finalize kernels after the projection.
-static cudaError_t launch_combine(const FwdLaunch& p) {
+cudaError_t launch_forward_combine(const FwdLaunch& p) {
   const int n_tiles = (p.V + kBN - 1) / kBN;
   const bool none = p.reduction == FLCE_REDUCTION_NONE;
   cudaError_t e = launch_combine_rows(p.part_m, p.part_s, p.zy, p.target, p.T, p.V, n_tiles,
@@ -131,19 +127,21 @@ cudaError_t launch_forward_bf16(const CUtensorMap& tx, const CUtensorMap& tw, co
     g.num_problems = 1;
     g.status = p.status;
     g.tile_counter = p.tile_counter;
-    FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V};
+    FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V, 0};
     cudaError_t e = launch_pair_core<FwdEpi, NoEpi, 2>(core, tx, tw, tx, tw, g, ea, NoEpi::Args{},
                                                        p.sms, p.stream, FLCE_ROLE_FORWARD);
     if (e != cudaSuccess) return e;
-    return launch_combine(p);
+    return launch_forward_combine(p);
   }
-  return launch_forward<false>(tx, tw, tx, tw, p);
+  cudaError_t e = launch_projection<false>(tx, tw, tx, tw, p, 0, p.V);
+  if (e != cudaSuccess) return e;
+  return launch_forward_combine(p);
 }
 
 cudaError_t launch_forward_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
                                 const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
-                                const FwdLaunch& p) {
-  return launch_forward<true>(tx_hi, tw_hi, tx_lo, tw_lo, p);
+                                const FwdLaunch& p, int col0, int cols) {
+  return launch_projection<true>(tx_hi, tw_hi, tx_lo, tw_lo, p, col0, cols);
 }
 
 }  // namespace flce

@@ -106,11 +106,16 @@ struct FwdLaunch {
   int sms;
   cudaStream_t stream;
 };
-// x/W maps: K-major boxes {64 x 128} (x) and {64 x 256} (W); tf32 adds lo copies.
+// bf16: projection over all V columns, then the combine. x/W maps: K-major boxes sized for the
+// forward role's core.
 cudaError_t launch_forward_bf16(const CUtensorMap& tx, const CUtensorMap& tw, const FwdLaunch& p);
+// tf32: the projection over vocab columns [col0, col0 + cols) only (col0 a multiple of 256);
+// the W maps (hi/lo, K-major {32 x 256}) cover those rows. launch_forward_combine follows the
+// last one.
 cudaError_t launch_forward_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
                                 const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
-                                const FwdLaunch& p);
+                                const FwdLaunch& p, int col0, int cols);
+cudaError_t launch_forward_combine(const FwdLaunch& p);
 
 // Merge the per-vocab-tile partials of `rows` tokens (all pointers already offset to those rows)
 // into lse, one loss sum per 256 rows (block_sums) and, if per_token is non-null, l[t].

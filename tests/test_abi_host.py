@@ -366,7 +366,7 @@ def test_sizing_rules_hold_on_random_shapes(lib):
             label = f"T={T} H={H} V={V} dtype={dt}"
             vc = B.flce_backward_slab_width(T, H, V, dt)
             n = -(-V // vc)
-            per_col = 2 * T if dt == B.FLCE_DTYPE_BF16 else 16 * up(T, 4)
+            per_col = 2 * T if dt == B.FLCE_DTYPE_BF16 else 16 * up(T, 4) + 16 * H
             vc_max = max(256, budget_slab // per_col // 256 * 256)
             assert vc % 256 == 0 and 256 <= vc <= up(V, 256), label
             assert (n - 1) * vc < V <= n * vc, label
@@ -378,10 +378,18 @@ def test_sizing_rules_hold_on_random_shapes(lib):
                 need = 2 * T * vc + (4 * T * H if n > 1 else 0)
                 assert need <= bws <= need + 4096, label
             else:
-                assert bws >= 8 * T * vc + 4 * vc * up(T, 4) * 2, label
+                # dz hi/lo in both orientations, x hi/lo in both, one weight slab's hi/lo in
+                # both: O((T + Vc) H), never O(V H)
+                need = 8 * T * vc + 8 * vc * up(T, 4) + 8 * T * H + 8 * H * up(T, 4) \
+                    + 8 * vc * H + 8 * H * up(vc, 4)
+                assert need <= bws <= need + 8192, label
             fws = B.flce_forward_workspace_size(T, H, V, dt)
             nt = -(-V // 256)
             assert 8 * nt * T + 4 * T <= fws, label
+            if dt == B.FLCE_DTYPE_F32:  # x hi/lo and one weight slab of at most 256 MB of copies
+                vf_max = max(256, (1 << 28) // (8 * H) // 256 * 256)
+                assert fws <= 8 * nt * T + 4 * T + 8 * T * H + 8 * min(vf_max, up(V, 256)) * H \
+                    + 4 * (T // 256 + 1) + 8192, label
             c = B.flce_forward_backward_chunk_tokens(T, H, V, dt)
             if dt != B.FLCE_DTYPE_BF16 or T < 512:
                 assert c == T, label

@@ -203,6 +203,7 @@ def test_contraction_cores_agree():
     (129, 8, 300, "bf16"),    # one row in the second token tile, smallest bf16 row
     (257, 72, 513, "f32"),    # ragged everywhere, H not a multiple of the K block
     (300, 200, 4096, "bf16"),
+    (300, 4096, 20000, "f32"),  # fp32 forward in 3 weight slabs of 6912 rows (256 MB of copies)
 ])
 def test_parity_edge_shapes(T, H, V, dtype):
     inp = make_inputs("tiny", T=T, H=H, V=V, dtype=dtype, seed=7 + T + V)
