@@ -113,8 +113,10 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
 // "[example] fused_linear_cross_entropy kernel" (Helion PR #1268), forward: a tiled matmul
 // feeding an online softmax that yields the log-sum-exp and the target logit of each row.
 // Each (vocab tile, token) pair leaves a partial (max m, sum of exp(z - m)) that the combine
-// kernel merges in a fixed order; the one tile holding target[t] also writes z[t, target[t]].
-// Vocab columns >= V are masked to -inf.
+// kernel merges in a fixed order; the one tile holding target[t] also writes z[t, target[t]]
+// and sx[t], its sum of exp(z - m) without the target column, from which the combine forms
+// the per-token loss without cancellation when the target dominates its row. Vocab columns
+// >= V are masked to -inf.
 // A tile's partial is formed from its two 128-column halves (chunks 0-3 and 4-7), each folded
 // chunk by chunk, then merged: half 1 into half 0. One warp does both halves, or two warps one
 // each (split 2, half 1 passed to half 0's warp through the exchange slots); the arithmetic,
@@ -125,13 +127,17 @@ struct FwdEpi {
     float* part_m;  // [n_tiles][T], n_tiles = ceil(V_total / 256)
     float* part_s;  // [n_tiles][T]
     float* zy;      // [T]
+    float* sx;      // [T]: the target tile's sum without the target column
     int T, V;       // V: vocab columns of this launch
     int col0;       // vocab column of the launch's first column (a multiple of 256)
   };
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
 
-  // Fold chunks [c_begin, c_end) of the tile into (m, s); picks up the target logit.
+  // Fold chunks [c_begin, c_end) of the tile into (m, s); picks up the target logit. With
+  // kExclude the target column's term is left out of s (the row's other columns are summed in
+  // exactly the same order, so a row whose target lies elsewhere gets the same s either way).
+  template <bool kExclude>
   static __device__ __forceinline__ void fold(const Args& a, const EpiCtx& ctx, int n0, int rel,
                                               int c_begin, int c_end, float& m, float& s,
                                               float& zy) {
@@ -149,7 +155,7 @@ struct FwdEpi {
           if (c0 + j >= a.V) v[j] = -INFINITY;
       }
       const int q = rel - c * 32;
-      if (q >= 0 && q < 32) {
+      if (!kExclude && q >= 0 && q < 32) {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (j == q) zy = v[j];
@@ -165,20 +171,47 @@ struct FwdEpi {
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {
-        s0 += ex2(fmaf(v[j + 0], kLog2e, -mnl));
-        s1 += ex2(fmaf(v[j + 1], kLog2e, -mnl));
-        s2 += ex2(fmaf(v[j + 2], kLog2e, -mnl));
-        s3 += ex2(fmaf(v[j + 3], kLog2e, -mnl));
+        float e0 = ex2(fmaf(v[j + 0], kLog2e, -mnl));
+        float e1 = ex2(fmaf(v[j + 1], kLog2e, -mnl));
+        float e2 = ex2(fmaf(v[j + 2], kLog2e, -mnl));
+        float e3 = ex2(fmaf(v[j + 3], kLog2e, -mnl));
+        if (kExclude) {
+          e0 = j + 0 == q ? 0.f : e0;
+          e1 = j + 1 == q ? 0.f : e1;
+          e2 = j + 2 == q ? 0.f : e2;
+          e3 = j + 3 == q ? 0.f : e3;
+        }
+        s0 += e0;
+        s1 += e1;
+        s2 += e2;
+        s3 += e3;
       }
       s = s * ex2((m - mn) * kLog2e) + ((s0 + s1) + (s2 + s3));
       m = mn;
     }
   }
 
-  // (m0, s0) <- the merge of half 0's and half 1's partials (half 1 may be empty: -inf, 0)
-  static __device__ __forceinline__ void merge(float& m0, float& s0, float m1, float s1) {
+  // Partial (m, s, sx) of chunks [c_begin, c_end): sx = s unless some row of the warp has its
+  // target there, when the chunks are folded once more without the target column (a few
+  // percent of tiles: the rows of a warp target 32 of the V / 256 tiles at most).
+  static __device__ __forceinline__ void half_partial(const Args& a, const EpiCtx& ctx, int n0,
+                                                      int rel, int c_begin, int c_end, float& m,
+                                                      float& s, float& sx, float& zy) {
+    fold<false>(a, ctx, n0, rel, c_begin, c_end, m, s, zy);
+    sx = s;
+    if (__any_sync(0xffffffffu, rel >= c_begin * 32 && rel < c_end * 32)) {
+      float mx, unused = 0.f;
+      fold<true>(a, ctx, n0, rel, c_begin, c_end, mx, sx, unused);
+    }
+  }
+
+  // Merge half 1's partial into half 0's (half 1 may be empty: -inf, 0, 0).
+  static __device__ __forceinline__ void merge(float& m0, float& s0, float& sx0, float m1,
+                                               float s1, float sx1) {
     const float mn = fmaxf(m0, m1);
-    s0 = s0 * ex2((m0 - mn) * kLog2e) + s1 * ex2((m1 - mn) * kLog2e);
+    const float f0 = ex2((m0 - mn) * kLog2e), f1 = ex2((m1 - mn) * kLog2e);
+    s0 = s0 * f0 + s1 * f1;
+    sx0 = sx0 * f0 + sx1 * f1;
     m0 = mn;
   }
 
@@ -191,30 +224,31 @@ struct FwdEpi {
     const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
     constexpr int kHalfChunks = kBN / 64;
     float zy = 0.f;
-    float m, s;
+    float m, s, sx;
     if (ctx.split == 1) {
-      float m1, s1;
-      fold(a, ctx, n0, rel, 0, kHalfChunks, m, s, zy);
-      fold(a, ctx, n0, rel, kHalfChunks, 2 * kHalfChunks, m1, s1, zy);
-      merge(m, s, m1, s1);
+      float m1, s1, sx1;
+      half_partial(a, ctx, n0, rel, 0, kHalfChunks, m, s, sx, zy);
+      half_partial(a, ctx, n0, rel, kHalfChunks, 2 * kHalfChunks, m1, s1, sx1, zy);
+      merge(m, s, sx, m1, s1, sx1);
     } else {
-      fold(a, ctx, n0, rel, ctx.c_begin, ctx.c_end, m, s, zy);
-      float2* slot = ctx.xchg + 32 * (ctx.iter & 1);
+      half_partial(a, ctx, n0, rel, ctx.c_begin, ctx.c_end, m, s, sx, zy);
+      float4* slot = ctx.xchg + 32 * (ctx.iter & 1);
       const int lane = ctx.row & 31;
       if (ctx.part == 1) {
-        slot[lane] = make_float2(m, s);
+        slot[lane] = make_float4(m, s, sx, 0.f);
         mbar_arrive(ctx.xbar);
       } else {
         if (!mbar_wait(ctx.xbar, static_cast<uint32_t>(ctx.iter & 1), ctx.status, ctx.abort))
           return;  // the partner left on the abort path: outputs are undefined anyway
-        const float2 o = slot[lane];
-        merge(m, s, o.x, o.y);
+        const float4 o = slot[lane];
+        merge(m, s, sx, o.x, o.y, o.z);
       }
     }
     if (valid && ctx.part == 0) {
       const size_t o = static_cast<size_t>(a.col0 / kBN + nb) * a.T + t;
       a.part_m[o] = m;
       a.part_s[o] = s;
+      if (rel >= 0) a.sx[t] = sx;
     }
     if (valid && rel >= ctx.c_begin * 32 && rel < ctx.c_end * 32) a.zy[t] = zy;
   }
@@ -223,7 +257,8 @@ struct FwdEpi {
 // ------------------------------------------------------------------------------- chunk logits
 // Single-call forward + backward over a chunk of tokens (the logits are computed once, not
 // recomputed): like FwdEpi, each (128-column vocab half-tile, token) pair leaves its (max m, sum
-// of exp(z - m)) partial and the tile holding target[t] writes z[t, target[t]]; in addition the
+// of exp(z - m)) partial and the half-tile holding target[t] writes z[t, target[t]] and its sum
+// without the target column; in addition the
 // half-tile's logits are kept, shifted by their maximum, as bf16 in a chunk buffer
 // zbuf[t][v] = z[t, v] - m. The shift puts the largest logits of each half-tile near 0, where
 // bf16 is most precise, so exp(zbuf + m - lse) recovers the dominant softmax terms accurately.
@@ -236,6 +271,7 @@ struct LogitsEpi {
     float* part_m;          // [2 n_tiles][T]: one partial per 128-column half-tile
     float* part_s;          // [2 n_tiles][T]
     float* zy;              // [T]
+    float* sx;              // [T]: the target half-tile's sum without the target column
     __nv_bfloat16* zbuf;    // [T][ldz]
     int ldz;
     int T, V;
@@ -281,11 +317,35 @@ struct LogitsEpi {
       store_rows_bf16x32(ctx.stage, v, ctx.row & 31, a.zbuf + c0, a.ldz, t - (ctx.row & 31),
                          a.T);
     }
+    const bool mine = rel >= h * 128 && rel < (h + 1) * 128;
+    float x0 = s0, x1 = s1;  // the sum without the target column (rows whose target is here)
+    if (__any_sync(0xffffffffu, mine)) {
+      x0 = 0.f;
+      x1 = 0.f;
+#pragma unroll 1
+      for (int c = h * kHalfChunks; c < (h + 1) * kHalfChunks; ++c) {
+        const int c0 = n0 + c * 32;
+        if (c0 >= a.V) break;
+        float v[32];
+        load_chunk(ctx, c, v);
+        const int q = rel - c * 32;
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float e0 = ex2(fmaf(v[j], kLog2e, -ml));
+          const float e1 = ex2(fmaf(v[j + 1], kLog2e, -ml));
+          x0 += (c0 + j < a.V && j != q) ? e0 : 0.f;
+          x1 += (c0 + j + 1 < a.V && j + 1 != q) ? e1 : 0.f;
+        }
+      }
+    }
     if (valid) {
       const size_t o = static_cast<size_t>(2 * nb + h) * a.T + t;
       a.part_m[o] = m;
       a.part_s[o] = s0 + s1;
-      if (rel >= h * 128 && rel < (h + 1) * 128) a.zy[t] = zy;
+      if (mine) {
+        a.zy[t] = zy;
+        a.sx[t] = x0 + x1;
+      }
     }
   }
 

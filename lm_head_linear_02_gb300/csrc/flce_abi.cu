@@ -190,7 +190,7 @@ struct Carver {
 };
 
 struct FwdWs {
-  float *part_m, *part_s, *zy, *block_sums;
+  float *part_m, *part_s, *zy, *sx, *block_sums;
   int* counter;                      // tile counter of the projection launch
   float *x_hi, *x_lo, *w_hi, *w_lo;  // f32 path only: x [T][H]; one weight slab [vf][H]
   int64_t vf;                        // f32 path: weight rows per projection launch
@@ -214,7 +214,8 @@ size_t carve_fwd(Carver& c, int64_t T, int64_t H, int64_t V, int dtype, FwdWs* w
   r.part_m = static_cast<float*>(c.take(sizeof(float) * nt * T));
   r.part_s = static_cast<float*>(c.take(sizeof(float) * nt * T));
   r.zy = static_cast<float*>(c.take(sizeof(float) * T));
-  r.block_sums = static_cast<float*>(c.take(sizeof(float) * cdiv(T, 256)));
+  r.sx = static_cast<float*>(c.take(sizeof(float) * T));
+  r.block_sums = static_cast<float*>(c.take(sizeof(float) * cdiv(T, flce::kLossBlockTokens)));
   r.counter = static_cast<int*>(c.take(sizeof(int)));
   if (dtype == FLCE_DTYPE_F32) {
     r.vf = fwd_slab_width_f32(H, V);
@@ -322,7 +323,7 @@ int64_t fused_chunk_rows(int64_t T, int64_t V) {
 struct FusedWs {
   int64_t rows, ldz, n_chunks;
   __nv_bfloat16* zbuf;
-  float *part_m, *part_s, *zy, *block_sums;
+  float *part_m, *part_s, *zy, *sx, *block_sums;
   int* counter;
 };
 
@@ -336,7 +337,8 @@ size_t carve_fused(Carver& c, int64_t T, int64_t H, int64_t V, FusedWs* w) {
   r.part_m = static_cast<float*>(c.take(sizeof(float) * nt * r.rows));
   r.part_s = static_cast<float*>(c.take(sizeof(float) * nt * r.rows));
   r.zy = static_cast<float*>(c.take(sizeof(float) * r.rows));
-  r.block_sums = static_cast<float*>(c.take(sizeof(float) * cdiv(T, 256)));
+  r.sx = static_cast<float*>(c.take(sizeof(float) * r.rows));
+  r.block_sums = static_cast<float*>(c.take(sizeof(float) * cdiv(T, flce::kLossBlockTokens)));
   r.counter = static_cast<int*>(c.take(sizeof(int)));
   if (w) *w = r;
   return c.off;
@@ -553,6 +555,7 @@ int flce_forward(const void* x, const void* weight, const int64_t* target, int64
   p.part_m = w.part_m;
   p.part_s = w.part_s;
   p.zy = w.zy;
+  p.sx = w.sx;
   p.block_sums = w.block_sums;
   p.lse = lse;
   p.loss = loss;
@@ -833,6 +836,7 @@ int flce_forward_backward(const void* x, const void* weight, const int64_t* targ
     cl.part_m = w.part_m;
     cl.part_s = w.part_s;
     cl.zy = w.zy;
+    cl.sx = w.sx;
     cl.grad_x_rows = static_cast<uint8_t*>(grad_x) + size_t(t0) * H * 2;
     cl.grad_w = grad_weight;
     cl.gw_mode = ci == 0 ? 0 : 4;  // written by the first chunk, summed in place after it
@@ -845,16 +849,19 @@ int flce_forward_backward(const void* x, const void* weight, const int64_t* targ
     cl.stream = s;
     e = flce::timed_launch(0, s, [&] { return flce::launch_chunk_logits(tx_k, tw_k, cl); });
     if (e == cudaSuccess)
-      e = flce::launch_combine_rows(w.part_m, w.part_s, w.zy, target + t0, int(rows), int(V),
-                                    int(w.ldz / (kTileN / 2)), lse + t0, w.block_sums + t0 / 256,
-                                    none ? loss + t0 : nullptr, status, s);
+      e = flce::launch_combine_rows(w.part_m, w.part_s, w.zy, w.sx, target + t0, int(rows),
+                                    int(V), int(w.ldz / (kTileN / 2)), kTileN / 2, lse + t0,
+                                    w.block_sums + t0 / flce::kLossBlockTokens,
+                                    none ? loss + t0 : nullptr, status,
+                                    s);
     if (e == cudaSuccess) e = flce::launch_form_dz(cl);
     if (e == cudaSuccess)
       e = flce::timed_launch(4, s,
                              [&] { return flce::launch_chunk_grads(tz_k, tw_mn, tz_mn, tx_mn, cl); });
   }
   if (e == cudaSuccess && !none)
-    e = flce::launch_finalize(w.block_sums, int(cdiv(T, 256)), int(T), reduction, loss, s);
+    e = flce::launch_finalize(w.block_sums, int(cdiv(T, flce::kLossBlockTokens)), int(T),
+                              reduction, loss, s);
   return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
 }
 

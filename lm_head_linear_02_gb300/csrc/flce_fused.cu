@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
                                 const ChunkLaunch& c) {
-  LogitsEpi::Args ea{c.target, c.part_m, c.part_s, c.zy, c.zbuf, c.ldz, c.rows, c.V};
+  LogitsEpi::Args ea{c.target, c.part_m, c.part_s, c.zy, c.sx, c.zbuf, c.ldz, c.rows, c.V};
   const Core core = role_core(c.sms, FLCE_ROLE_FORWARD);  // maps boxed for this core
   GemmGrid g{};
   g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, core_tile_rows(core), 0, true);

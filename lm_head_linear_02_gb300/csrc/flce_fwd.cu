@@ -7,52 +7,88 @@
 
 namespace flce {
 
-constexpr int kCombineThreads = 256;
+// The combine kernel: a block of 8 warps per 32 tokens; warp w merges the partials of the
+// w-th eighth of the vocab tiles for those tokens (lane = token, so every load of a tile's
+// partials is 32 consecutive tokens), then warp 0 merges the eight results in warp order.
+constexpr int kCombineWarps = 8;
+constexpr int kCombineThreads = 32 * kCombineWarps;
+constexpr int kCombineTokens = kLossBlockTokens;  // tokens per block and per loss block sum
 
-// Merge the per-(vocab tile) partials of each token in increasing tile order:
-//   M = max_i m_i,  S = sum_i s_i exp(m_i - M),  lse = M + ln S,  l = lse - z[t, target[t]].
-// Writes lse[t] and one partial loss sum per block (fixed-order tree); with per_token non-null
-// (the 'none' reduction) it also writes l[t] there.
+// One partial into the running (M, S, SX): S sums exp(z - M) over every column seen, SX over
+// every column but the target.
+__device__ __forceinline__ void lse_merge(float& M, float& S, float& SX, float m, float s,
+                                          float s_x) {
+  const float mn = fmaxf(M, m);
+  const float f0 = ex2((M - mn) * kLog2e), f1 = ex2((m - mn) * kLog2e);
+  S = S * f0 + s * f1;
+  SX = SX * f0 + s_x * f1;
+  M = mn;
+}
+
+// Merge the per-(vocab tile) partials of each token in a fixed order (eighths of the tile
+// range, each in increasing tile order, then the eighths in order):
+//   M = max_i m_i,  S = sum_i s_i exp(m_i - M),  lse = M + ln S,
+// and, with the target tile's sum taken without the target column (sx), the same merge SX of
+// the terms of every column but the target. The per-token loss l = lse - z[t, target[t]] is
+// formed as ln(1 + SX) when the target logit is the row maximum (then lse and z[t, target[t]]
+// nearly cancel and l is close to 0), else as (M - z[t, target[t]]) + ln S.
+// Writes lse[t] and one partial loss sum per 32 tokens (fixed-order shuffle tree); with
+// per_token non-null (the 'none' reduction) it also writes l[t] there. tile_cols: vocab columns
+// per partial.
 __global__ void __launch_bounds__(kCombineThreads)
     k_fwd_combine(const float* __restrict__ part_m, const float* __restrict__ part_s,
-                  const float* __restrict__ zy, const int64_t* __restrict__ target, int T, int V,
-                  int n_tiles, float* __restrict__ lse, float* __restrict__ block_sums,
+                  const float* __restrict__ zy, const float* __restrict__ sx,
+                  const int64_t* __restrict__ target, int T, int V, int n_tiles, int tile_cols,
+                  float* __restrict__ lse, float* __restrict__ block_sums,
                   float* __restrict__ per_token, int* status) {
-  const int t = blockIdx.x * kCombineThreads + threadIdx.x;
-  float l = 0.f;
-  if (t < T) {
-    float M = -INFINITY, S = 0.f;
-    for (int i = 0; i < n_tiles; ++i) {
+  __shared__ float3 partial[kCombineWarps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kCombineTokens + lane;
+  const bool valid = t < T;
+  const int64_t y = valid ? target[t] : -1;
+  const bool in_range = y >= 0 && y < V;
+  const int ty = in_range ? static_cast<int>(y / tile_cols) : -1;
+  const int per_warp = (n_tiles + kCombineWarps - 1) / kCombineWarps;
+  const int i0 = warp * per_warp;
+  const int i1 = min(n_tiles, i0 + per_warp);
+  float M = -INFINITY, S = 0.f, SX = 0.f;
+  if (valid) {
+    const float sxt = (ty >= i0 && ty < i1) ? sx[t] : 0.f;
+    for (int i = i0; i < i1; ++i) {
       const float m = part_m[static_cast<size_t>(i) * T + t];
       const float s = part_s[static_cast<size_t>(i) * T + t];
       if (m == -INFINITY) continue;  // an empty partial (a half-tile wholly beyond V)
-      const float mn = fmaxf(M, m);
-      S = S * ex2((M - mn) * kLog2e) + s * ex2((m - mn) * kLog2e);
-      M = mn;
+      lse_merge(M, S, SX, m, s, i == ty ? sxt : s);
     }
-    const float lse_t = M + logf(S);
-    lse[t] = lse_t;
-    const int64_t y = target[t];
-    if (y < 0 || y >= V) {
+  }
+  partial[warp][lane] = make_float3(M, S, SX);
+  __syncthreads();
+  if (warp != 0) return;
+  M = -INFINITY;
+  S = 0.f;
+  SX = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineWarps; ++w) {
+    const float3 p = partial[w][lane];
+    if (p.x != -INFINITY) lse_merge(M, S, SX, p.x, p.y, p.z);
+  }
+  float l = 0.f;
+  if (valid) {
+    const float lnS = logf(S);
+    lse[t] = M + lnS;
+    if (!in_range) {
       atomicOr(status, FLCE_STATUS_TARGET_RANGE);
       l = __int_as_float(0x7fc00000);  // NaN
     } else {
-      l = lse_t - zy[t];
+      const float z_y = zy[t];
+      l = z_y == M ? log1pf(SX) : (M - z_y) + lnS;
     }
     if (per_token) per_token[t] = l;
   }
-  // Fixed-order block reduction: shuffle tree within each warp, then over the warp sums.
-  __shared__ float warp_sums[kCombineThreads / 32];
+  // Fixed-order reduction of the block's 32 per-token losses.
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_down_sync(0xffffffffu, l, o);
-  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = l;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float w = threadIdx.x < kCombineThreads / 32 ? warp_sums[threadIdx.x] : 0.f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) w += __shfl_down_sync(0xffffffffu, w, o);
-    if (threadIdx.x == 0) block_sums[blockIdx.x] = w;
-  }
+  if (lane == 0) block_sums[blockIdx.x] = l;
 }
 
 // loss = sum of the block sums (fp64, fixed order), divided by T for the mean reduction.
@@ -86,7 +122,7 @@ static cudaError_t launch_projection(const CUtensorMap& tx, const CUtensorMap& t
   g.num_problems = 1;
   g.status = p.status;
   g.tile_counter = p.tile_counter;
-  FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, cols, col0};
+  FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.sx, p.T, cols, col0};
   return launch_gemm<kTF32, FwdEpi, NoEpi>(tx, tw, tx_lo, tw_lo, g, ea, NoEpi::Args{}, p.sms,
                                            p.stream);
 }
@@ -95,21 +131,22 @@ static cudaError_t launch_projection(const CUtensorMap& tx, const CUtensorMap& t
 cudaError_t launch_forward_combine(const FwdLaunch& p) {
   const int n_tiles = (p.V + kBN - 1) / kBN;
   const bool none = p.reduction == FLCE_REDUCTION_NONE;
-  cudaError_t e = launch_combine_rows(p.part_m, p.part_s, p.zy, p.target, p.T, p.V, n_tiles,
-                                      p.lse, p.block_sums, none ? p.loss : nullptr, p.status,
-                                      p.stream);
+  cudaError_t e = launch_combine_rows(p.part_m, p.part_s, p.zy, p.sx, p.target, p.T, p.V,
+                                      n_tiles, kBN, p.lse, p.block_sums, none ? p.loss : nullptr,
+                                      p.status, p.stream);
   if (e != cudaSuccess || none) return e;
-  return launch_finalize(p.block_sums, (p.T + kCombineThreads - 1) / kCombineThreads, p.T,
+  return launch_finalize(p.block_sums, (p.T + kCombineTokens - 1) / kCombineTokens, p.T,
                          p.reduction, p.loss, p.stream);
 }
 
 cudaError_t launch_combine_rows(const float* part_m, const float* part_s, const float* zy,
-                                const int64_t* target, int rows, int V, int n_tiles, float* lse,
-                                float* block_sums, float* per_token, int* status,
-                                cudaStream_t stream) {
-  const int nblk = (rows + kCombineThreads - 1) / kCombineThreads;
-  k_fwd_combine<<<nblk, kCombineThreads, 0, stream>>>(part_m, part_s, zy, target, rows, V, n_tiles,
-                                                      lse, block_sums, per_token, status);
+                                const float* sx, const int64_t* target, int rows, int V,
+                                int n_tiles, int tile_cols, float* lse, float* block_sums,
+                                float* per_token, int* status, cudaStream_t stream) {
+  const int nblk = (rows + kCombineTokens - 1) / kCombineTokens;
+  k_fwd_combine<<<nblk, kCombineThreads, 0, stream>>>(part_m, part_s, zy, sx, target, rows, V,
+                                                      n_tiles, tile_cols, lse, block_sums,
+                                                      per_token, status);
   return cudaGetLastError();
 }
 
@@ -127,7 +164,7 @@ cudaError_t launch_forward_bf16(const CUtensorMap& tx, const CUtensorMap& tw, co
     g.num_problems = 1;
     g.status = p.status;
     g.tile_counter = p.tile_counter;
-    FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.T, p.V, 0};
+    FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.sx, p.T, p.V, 0};
     cudaError_t e = launch_pair_core<FwdEpi, NoEpi, 2>(core, tx, tw, tx, tw, g, ea, NoEpi::Args{},
                                                        p.sms, p.stream, FLCE_ROLE_FORWARD);
     if (e != cudaSuccess) return e;

@@ -97,7 +97,8 @@ struct FwdLaunch {
   float* part_m;      // [n_tiles][T]
   float* part_s;      // [n_tiles][T]
   float* zy;          // [T]
-  float* block_sums;  // [ceil(T / 256)]
+  float* sx;          // [T]: the target tile's exp-sum without the target column
+  float* block_sums;  // [ceil(T / kLossBlockTokens)]
   float* lse;         // [T]
   float* loss;        // [1], or [T] for the 'none' reduction
   int* tile_counter;  // zeroed before the projection launch: tiles handed out in list order
@@ -117,12 +118,16 @@ cudaError_t launch_forward_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_
                                 const FwdLaunch& p, int col0, int cols);
 cudaError_t launch_forward_combine(const FwdLaunch& p);
 
-// Merge the per-vocab-tile partials of `rows` tokens (all pointers already offset to those rows)
-// into lse, one loss sum per 256 rows (block_sums) and, if per_token is non-null, l[t].
+// Tokens per loss block sum written by the combine kernel (chunks of the single call start at
+// multiples of 256 tokens, so at multiples of this).
+constexpr int kLossBlockTokens = 32;
+// Merge the per-vocab-tile partials of `rows` tokens (all pointers already offset to those rows;
+// tile_cols vocab columns per partial) into lse, one loss sum per kLossBlockTokens rows
+// (block_sums) and, if per_token is non-null, l[t].
 cudaError_t launch_combine_rows(const float* part_m, const float* part_s, const float* zy,
-                                const int64_t* target, int rows, int V, int n_tiles, float* lse,
-                                float* block_sums, float* per_token, int* status,
-                                cudaStream_t stream);
+                                const float* sx, const int64_t* target, int rows, int V,
+                                int n_tiles, int tile_cols, float* lse, float* block_sums,
+                                float* per_token, int* status, cudaStream_t stream);
 // loss[0] = sum of n_blocks block sums (fp64, fixed order), / T for the mean reduction.
 cudaError_t launch_finalize(const float* block_sums, int n_blocks, int T, int reduction,
                             float* loss, cudaStream_t stream);
@@ -193,7 +198,7 @@ struct ChunkLaunch {
   float scale;             // 1 or 1/T
   __nv_bfloat16* zbuf;     // [rows][ldz] chunk logits (shifted) / dz
   int ldz;
-  float *part_m, *part_s, *zy;  // [ldz / 128][rows] (one per half-tile) x 2, [rows]
+  float *part_m, *part_s, *zy, *sx;  // [ldz / 128][rows] (one per half-tile) x 2, [rows] x 2
   void* grad_x_rows;       // grad_x + t0 * H
   void* grad_w;
   int gw_mode;             // 0: the first chunk writes grad_w, 4: later chunks add to it

@@ -129,7 +129,7 @@ struct StageGeom {
 // [c_begin, c_end) of the block's 256 columns. With split = 2 two warps share the same rows and
 // take the column halves (part 0: chunks 0-3, part 1: chunks 4-7). An epilogue that needs
 // per-row results of both halves passes them from part 1 to part 0 through xchg (two sets of
-// 32 float2 slots, alternating with `iter`, the warp's tile count) and the mbarrier xbar (32
+// 32 float4 slots, alternating with `iter`, the warp's tile count) and the mbarrier xbar (32
 // arrivals per tile, phase parity iter & 1): part 1 writes and arrives, part 0 waits, bounded
 // like every pipeline wait, so a partner that left on the abort path cannot hang it.
 struct EpiCtx {
@@ -142,7 +142,7 @@ struct EpiCtx {
   int two_acc;        // 1: the tile is the sum of two accumulators, taddr and taddr_corr
   uint32_t taddr_corr;
   uint32_t xbar;      // exchange mbarrier of the two warps sharing rows (split 2)
-  float2* xchg;       // exchange slots of those two warps (split 2)
+  float4* xchg;       // exchange slots of those two warps (split 2)
   int* status;        // device status word (a timed-out exchange sets FLCE_STATUS_TIMEOUT)
   volatile int* abort;
 };

@@ -304,7 +304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
     // the part-0 warp of this row block lends the exchange slots (epilogues that combine
     // per-row partials across the two parts do not use store staging)
     const int e_part0 = 4 * half + ((quarter - 2) & 3);
-    float2* xchg = reinterpret_cast<float2*>(smem + kPairRingBytes + 1024 +
+    float4* xchg = reinterpret_cast<float4*>(smem + kPairRingBytes + 1024 +
                                              static_cast<uint32_t>(e_part0) * kEpiStageBytes);
     int acc = 0;
     uint32_t acc_phase = 0;

@@ -388,8 +388,8 @@ def test_sizing_rules_hold_on_random_shapes(lib):
             assert 8 * nt * T + 4 * T <= fws, label
             if dt == B.FLCE_DTYPE_F32:  # x hi/lo and one weight slab of at most 256 MB of copies
                 vf_max = max(256, (1 << 28) // (8 * H) // 256 * 256)
-                assert fws <= 8 * nt * T + 4 * T + 8 * T * H + 8 * min(vf_max, up(V, 256)) * H \
-                    + 4 * (T // 256 + 1) + 8192, label
+                assert fws <= 8 * nt * T + 8 * T + 8 * T * H + 8 * min(vf_max, up(V, 256)) * H \
+                    + 4 * (T // 32 + 1) + 8192, label
             c = B.flce_forward_backward_chunk_tokens(T, H, V, dt)
             if dt != B.FLCE_DTYPE_BF16 or T < 512:
                 assert c == T, label
@@ -403,7 +403,8 @@ def test_sizing_rules_hold_on_random_shapes(lib):
             assert c - (T - (k - 1) * c) <= 256 * k, label
             fbs = B.flce_forward_backward_workspace_size(T, H, V, dt)
             need = 2 * c * ldz + 2 * 4 * (ldz // 128) * c  # chunk logits + half-tile partials
-            assert need <= fbs <= need + 4 * c + 4 * (T // 256 + 1) + 4096, label
+            # plus per-row target logit and target-excluded sum, block sums, tile counter
+            assert need <= fbs <= need + 8 * c + 4 * (T // 32 + 1) + 6 * 256, label
 
 
 def test_missing_library_fails_loudly(lib, monkeypatch, tmp_path):

@@ -644,7 +644,9 @@ def _check_peaked(inp, gl, ref, reduction, loss, lse, gx, gw, label):
         zy0 = ref["lse"] - ref["loss"]
         floor = 2.0 ** -22 * (np.abs(ref["lse"]) + np.abs(zy0))
         excess = np.abs(loss - ref["loss"]) - (tol["loss"] * np.abs(ref["loss"]) + floor)
-        e_loss = float(np.max(np.abs(loss - ref["loss"]) / np.maximum(np.abs(ref["loss"]), 1e-30)))
+        # reported: the relative error, with the floor in place of |l0| where |l0| is smaller
+        # (there even the float64 oracle's lse - z_y carries a rounding of that size)
+        e_loss = float(np.max(np.abs(loss - ref["loss"]) / np.maximum(np.abs(ref["loss"]), floor)))
         ok_loss = bool(np.all(excess <= 0))
     else:
         e_loss = abs(loss - ref["loss"]) / abs(ref["loss"])
