@@ -219,12 +219,11 @@ int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_RO
  *                          128-row CTA tiles but leaves no TMEM for overlapping a tile's
  *                          epilogue with the next tile. A bit mask of FLCE_ROLE_*; -1 (the
  *                          default) picks a measured mask. Roles not on SM pairs ignore it.
- *   FLCE_TUNE_RASTER_VOCAB vocabulary rows per raster group of the contractions whose N
- *                          dimension is the vocabulary (the forward projection, the backward's
- *                          dz and the single call's chunk logits): tiles sweep the token rows
- *                          inside a group, so the group's weight rows stay in L2 while x streams
- *                          past. Multiple of 256; 0 (the default) rasters those contractions
- *                          over token rows as well (FLCE_TUNE_RASTER_ROWS).
+ *   FLCE_TUNE_RASTER_VOCAB vocabulary rows per raster group of the forward projection and
+ *                          the backward's dz contraction (whose N dimension is the vocabulary):
+ *                          tiles sweep the token rows inside a group, so the group's weight rows
+ *                          stay in L2 while x streams past. Multiple of 256; default 4096; 0
+ *                          rasters them over token rows instead (FLCE_TUNE_RASTER_ROWS).
  *   FLCE_TUNE_SPLIT_EPILOGUE which roles on wide pair tiles drain each finished 128-row block
  *                          with two epilogue warps of 128 columns each (16 epilogue warps per
  *                          CTA) instead of one of 256: the single accumulator of a wide tile is

@@ -63,7 +63,8 @@ cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
   LogitsEpi::Args ea{c.target, c.part_m, c.part_s, c.zy, c.sx, c.zbuf, c.ldz, c.rows, c.V};
   const Core core = role_core(c.sms, FLCE_ROLE_FORWARD);  // maps boxed for this core
   GemmGrid g{};
-  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, core_tile_rows(core), 0, true);
+  // token-row raster: a chunk's x rows (at most a few thousand) are what stays in L2 here
+  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, core_tile_rows(core), 0, false);
   g.num_problems = 1;
   g.status = c.status;
   g.tile_counter = c.tile_counter;  // tiles in list order: the pairs sharing a W tile stay in step

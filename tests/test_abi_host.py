@@ -211,13 +211,13 @@ def test_tuning_knobs_validate(lib):
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
     assert B.flce_get_tuning(B.FLCE_TUNE_WIDE_TILES) == 7
-    # vocabulary raster groups: off by default, multiples of 256 when set
-    assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_VOCAB) == 0
-    B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 8192)
+    # vocabulary raster groups: 4096 rows by default, multiples of 256 (0: token raster)
+    assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_VOCAB) == 4096
+    B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 0)
     try:
-        assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_VOCAB) == 8192
+        assert B.flce_get_tuning(B.FLCE_TUNE_RASTER_VOCAB) == 0
     finally:
-        B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 0)
+        B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 4096)
     # two epilogue warps per row block: off by default; -1 restores the default
     assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == 0
     B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, B.FLCE_ROLE_FORWARD | B.FLCE_ROLE_DZ)

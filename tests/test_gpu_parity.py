@@ -169,8 +169,8 @@ def test_contraction_cores_agree():
     x, w, y = to_device(inp)
     outs, fused = [], []
     try:
-        for pair, wide, split, rv in [(0, 0, -1, 0), (7, 0, -1, 0), (7, 7, -1, 0), (7, 7, 3, 0),
-                                      (7, 7, -1, 1024)]:
+        for pair, wide, split, rv in [(0, 0, -1, 4096), (7, 0, -1, 4096), (7, 7, -1, 4096),
+                                      (7, 7, 3, 4096), (7, 7, -1, 0), (7, 7, -1, 1024)]:
             B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
             B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
             B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, split)
@@ -187,7 +187,7 @@ def test_contraction_cores_agree():
         B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
         B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
-        B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 0)
+        B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 4096)
     for other in outs[1:]:
         for a, b in zip(outs[0], other):
             assert np.array_equal(a, b)
