@@ -56,6 +56,23 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
+# --tune NAME=VALUE: the library's process-wide tuning keys (include/flce.h, FLCE_TUNE_*)
+TUNING_KEYS = {"raster_rows": "FLCE_TUNE_RASTER_ROWS", "sm_pairs": "FLCE_TUNE_SM_PAIRS",
+               "wide_tiles": "FLCE_TUNE_WIDE_TILES", "raster_vocab": "FLCE_TUNE_RASTER_VOCAB",
+               "split_epilogue": "FLCE_TUNE_SPLIT_EPILOGUE", "chunk_bytes": "FLCE_TUNE_CHUNK_BYTES"}
+
+
+def parse_tuning(items):
+    """['raster_vocab=4096', ...] -> {'raster_vocab': 4096, ...} (names checked, values int)."""
+    out = {}
+    for item in items:
+        name, sep, value = item.partition("=")
+        if not sep or name not in TUNING_KEYS:
+            raise ValueError(f"--tune expects NAME=VALUE with NAME in {sorted(TUNING_KEYS)}")
+        out[name] = int(value, 0)
+    return out
+
+
 def max_over_ranks(value: float, dist, device=None) -> float:
     """The largest of each rank's value (a timed region ends when the slowest rank is done).
     Single-process runs (dist None) return the value itself."""
@@ -318,6 +335,8 @@ def run_ours(args, wl, rank: int, world: int, dist):
     if not build_mod.up_to_date():
         raise RuntimeError("libflce.so is missing or stale: run __graft_entry__.build() first")
     B.lib()
+    for name, value in args.tuning.items():
+        B.flce_set_tuning(getattr(B, TUNING_KEYS[name]), value)
 
     t_gen = time.perf_counter()
     inp = make_inputs(wl)
@@ -558,7 +577,9 @@ def run_ours(args, wl, rank: int, world: int, dist):
                        sm_pair_roles=[n for n, b in (("forward", 1), ("dz", 2), ("grads", 4))
                                       if pair_roles & b],
                        wide_tile_roles=[n for n, b in (("forward", 1), ("dz", 2), ("grads", 4))
-                                        if wide_roles & b]),
+                                        if wide_roles & b],
+                       tuning={name: B.flce_get_tuning(getattr(B, key))
+                               for name, key in TUNING_KEYS.items() if name != "sm_pairs"}),
         "fwd_ms": statistics.median(fwd_ms), "bwd_ms": statistics.median(bwd_ms),
         "fwd_tokens_per_s": T / (statistics.median(fwd_ms) * 1e-3),
         "tensor_tflops_step": step_tflops,
@@ -615,9 +636,16 @@ def main():
                     help="skip the PyTorch eager context measurement")
     ap.add_argument("--oracle-tokens", type=int, default=64,
                     help="token sample per oracle step (CPU baseline / reference arm)")
+    ap.add_argument("--tune", action="append", default=[], metavar="NAME=VALUE",
+                    help="set a libflce tuning key before timing (repeatable): " +
+                         ", ".join(sorted(TUNING_KEYS)))
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    try:
+        args.tuning = parse_tuning(args.tune)
+    except ValueError as exc:
+        ap.error(str(exc))
     wl = WORKLOADS[args.workload]
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -9,6 +9,8 @@ import os
 import subprocess
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 BENCH = os.path.join(ROOT, "bench.py")
 
@@ -76,3 +78,13 @@ def test_cpu_baseline_times_at_least_the_bounded_duration():
     elapsed = done / cb["value"]
     assert elapsed >= 0.3
     assert abs(elapsed - secs) <= 0.051  # the sample text prints the seconds to 0.1
+
+
+def test_tuning_arguments_parse_and_refuse_unknown_names():
+    import bench
+
+    assert bench.parse_tuning(["raster_vocab=4096", "chunk_bytes=0x40000000"]) == {
+        "raster_vocab": 4096, "chunk_bytes": 1 << 30}
+    for bad in (["raster_vocab"], ["nonsense=1"], ["raster_vocab=abc"]):
+        with pytest.raises(ValueError):
+            bench.parse_tuning(bad)
