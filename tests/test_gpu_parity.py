@@ -291,8 +291,8 @@ def test_out_of_range_target_sets_status_and_nan_loss():
         A.check_status(status)
 
 
-@pytest.mark.parametrize("pair,wide", [(0, 0), (7, 0), (7, 7)])
-def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide):
+@pytest.mark.parametrize("pair,wide,split", [(0, 0, -1), (7, 0, -1), (7, 7, -1), (7, 7, 3)])
+def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide, split):
     """A withheld pipeline signal ends the launch with FLCE_STATUS_TIMEOUT after the bounded wait
     (about 2 s) instead of hanging, on each contraction core (single SM, SM pairs with 128-row
     and with 256-row CTA tiles, whose abort path also drains the partner CTA); the next calls
@@ -303,6 +303,7 @@ def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide):
     x, w, y = to_device(inp)
     B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
     B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
+    B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, split)
     try:
         B.flce_test_withhold_signal()
         t0 = time.time()
@@ -316,7 +317,8 @@ def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide):
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
-    assert_full_parity(inp, "mean", label=f"after timeout pair={pair} wide={wide}")
+        B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
+    assert_full_parity(inp, "mean", label=f"after timeout pair={pair} wide={wide} split={split}")
 
 
 def test_sum_mean_and_grad_loss_scaling():
@@ -590,6 +592,30 @@ def test_single_call_gradient_tiles_single_sm_and_sm_pairs(pair, wide):
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
+
+
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_single_call_many_chunks(reduction):
+    """A chunk budget of 256 token rows' logits splits the ragged workload into 5 chunks (4 x 256
+    + 245): grad_weight is written by the first and summed in place, in bf16, by four more."""
+    inp = make_inputs("ragged", dtype="bf16")
+    T, H, V = inp.workload.T, inp.workload.H, inp.workload.V
+    ldz = -(-V // 256) * 256
+    B.flce_set_tuning(B.FLCE_TUNE_CHUNK_BYTES, 2 * 256 * ldz)
+    try:
+        assert B.flce_forward_backward_chunk_tokens(T, H, V, B.FLCE_DTYPE_BF16) == 256
+        gl = np.random.default_rng(8).standard_normal(T) if reduction == "none" else 0.5
+        x, w, y = to_device(inp)
+        loss, lse, gx, gw = run_fused(x, w, y, reduction, gl)
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_CHUNK_BYTES, 0)
+    ref = oracle.flce(inp.x, inp.weight, inp.target, reduction, grad_loss=gl)
+    tol = TOL["bf16"]
+    rel = (float(np.max(np.abs(loss - ref["loss"]) / np.abs(ref["loss"]))) if reduction == "none"
+           else abs(loss - ref["loss"]) / abs(ref["loss"]))
+    e_gx, e_gw = norm_err(gx, ref["grad_x"]), norm_err(gw, ref["grad_weight"])
+    print(f"single call, 5 chunks, {reduction}: loss {rel:.3e} gx {e_gx:.3e} gw {e_gw:.3e}")
+    assert rel <= tol["loss"] and e_gx <= tol["grad"] and e_gw <= tol["grad"]
 
 
 def test_single_call_is_deterministic_and_agrees_with_two_calls():
