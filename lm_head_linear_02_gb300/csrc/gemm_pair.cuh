@@ -15,7 +15,7 @@
 //                busy; the price is one accumulator filling all 512 TMEM columns, so the epilogue
 //                of a tile is not hidden behind the next main loop (8 epilogue warps halve it).
 //
-// Roles (per CTA: 2 + 4 kRows / 128 warps):
+// Roles (per CTA: 2 + 4 (kRows / 128) kSplit warps):
 //   warp 0 (both CTAs)   TMA producer: loads this CTA's A rows and B half; completion is counted
 //                        on the LEADER's full barrier, which the leader arms for both CTAs.
 //   warp 1 (leader)      MMA issuer: waits for both CTAs' bytes, issues M=256 N=256 MMAs, and
@@ -23,7 +23,9 @@
 //   warp 1 (peer)        idle (takes part in the pair's TMEM allocation only).
 //   warps 2.. (both)     epilogue: warp 2 + 4h + q drains TMEM lanes [32q', 32q' + 32) of half h
 //                        (q' = warp % 4, the lane quarter a warp may access), then tells the
-//                        leader (remote mbarrier arrive) that the accumulator is free.
+//                        leader (remote mbarrier arrive) that the accumulator is free. With
+//                        kSplit = 2 a second set of warps (2 + 4 kHalves + ...) takes columns
+//                        128-255 of the same rows and the first set columns 0-127.
 // A launch may carry two independent problems: grad_W and grad_x of one vocab slab run together,
 // so that their tiles fill the GPU in one wave pattern instead of two.
 #pragma once
