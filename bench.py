@@ -546,6 +546,12 @@ def run_ours(args, wl, rank: int, world: int, dist):
     peaks, peak_kind = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if wl.dtype == "f32":
+        # fp32 inputs run as three TF32 products per algorithmic FLOP (3xTF32): the peak is the
+        # measured bf16 one times the nominal dense TF32/bf16 ratio (1.1 / 2.25 PFLOP/s), / 3
+        peak_burst *= (1.1 / 2.25) / 3.0
+        peak_sus *= (1.1 / 2.25) / 3.0
+        peak_kind = peak_kind + ", TF32 = 1.1/2.25 of bf16, / 3 products per FLOP"
     # each role's algorithmic FLOPs per step: one T x H x V contraction, two for the launches
     # that run grad_weight and grad_x together
     role_flops = {r: args.steps * roofline.flops(T, H, V, "fwd") * (2 if r == "backward_grads" else 1)

@@ -11,8 +11,8 @@ Workloads are the LM-head shapes of the pages' benchmarks:
   hidden 4096, tokens in {4096, 8192, 16384, 32768}, bf16.
 * "feat(FLCE): add helion version of fused linear cross entropy" (Liger-Kernel PR #928), the
   failing-test list: (B, T, H, V) = (2, 1024, 4096, 32000) and (3, 423, 1000, 10000); and its
-  benchmark tables for a Qwen3 head (H=4096, V=151936, BT=32768) and a Gemma3 head (H=2304,
-  V=262208, BT=8192).
+  benchmark tables for a Qwen3 head (H=4096, V=151936, BT=32768), a Gemma3 head (H=2304,
+  V=262208, BT=8192) and an fp32 head (H=4096, V=32000, BT=32768).
 
 The pages ship no datasets; these synthetic draws stand in for the benchmark scripts' random
 activations and weights: x ~ N(0, 1), weight ~ N(0, 0.02^2), and targets either uniform over the
@@ -91,6 +91,8 @@ WORKLOADS = {
                  note="Qwen3-sized head"),
         Workload("gemma3_head_t8192", 7, 8192, 2304, 262208, "bf16", "uniform", ("mean",),
                  note="Gemma3-sized head: narrow hidden, very wide vocabulary"),
+        Workload("fp32_head_t32768", 11, 32768, 4096, 32000, "f32", "uniform", ("mean",),
+                 note="fp32 head of the Liger-Kernel PR's fp32 tables (T=32768, V=32000)"),
         Workload("spread", 8, 1100, 1024, 8000, "bf16", "uniform", ("sum", "mean", "none"),
                  w_std=0.3, note="logits of standard deviation ~10: a peaked softmax"),
         Workload("confident", 9, 1100, 1024, 8000, "bf16", "uniform", ("sum", "mean", "none"),
