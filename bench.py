@@ -564,7 +564,15 @@ def run_ours(args, wl, rank: int, world: int, dist):
     step_tflops = roofline.flops(T, H, V, "fwd_bwd") / (ms_step * 1e-3) / 1e12
     # forward: projection kernel + combine + finalize; backward per slab: dz and one launch for
     # both gradients (bf16), or dz, grad_W and grad_x plus 6 TF32 operand splits (fp32).
-    launches_per_step = (3 + 2 * n_slabs) if wl.dtype == "bf16" else (9 + 3 * n_slabs)
+    # Kernels of the library launched per step, from the contraction launches the timing hooks
+    # counted: bf16 - projection, combine, finalize, then per vocab slab dz and one gradient
+    # launch; fp32 - the x split, per weight slab a split and a projection, combine, finalize,
+    # then two x splits and per vocab slab two weight splits, dz, grad_W and grad_x.
+    fwd_launches = per_role["forward"][0] // args.steps
+    if wl.dtype == "bf16":
+        launches_per_step = fwd_launches + 2 + 2 * n_slabs
+    else:
+        launches_per_step = 1 + 2 * fwd_launches + 2 + 2 + 5 * n_slabs
     cpu = cpu_baseline(inp, args.oracle_tokens) if world == 1 else None
     context = None
     if world == 1 and not args.no_context:
