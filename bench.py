@@ -59,7 +59,8 @@ def log(*a):
 # --tune NAME=VALUE: the library's process-wide tuning keys (include/flce.h, FLCE_TUNE_*)
 TUNING_KEYS = {"raster_rows": "FLCE_TUNE_RASTER_ROWS", "sm_pairs": "FLCE_TUNE_SM_PAIRS",
                "wide_tiles": "FLCE_TUNE_WIDE_TILES", "raster_vocab": "FLCE_TUNE_RASTER_VOCAB",
-               "split_epilogue": "FLCE_TUNE_SPLIT_EPILOGUE", "chunk_bytes": "FLCE_TUNE_CHUNK_BYTES"}
+               "split_epilogue": "FLCE_TUNE_SPLIT_EPILOGUE", "chunk_bytes": "FLCE_TUNE_CHUNK_BYTES",
+               "ordered_drain": "FLCE_TUNE_ORDERED_DRAIN"}
 
 
 def parse_tuning(items):

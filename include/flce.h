@@ -231,6 +231,13 @@ int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_RO
  *                          of FLCE_ROLE_FORWARD (forward projection and single-call chunk
  *                          logits) and FLCE_ROLE_DZ; FLCE_ROLE_GRADS is ignored. -1 restores
  *                          the default, 0 (measured no faster on GB300).
+ *   FLCE_TUNE_ORDERED_DRAIN which roles on wide pair tiles (with one epilogue warp per row
+ *                          block) drain a finished tile's two 128-row halves one after the
+ *                          other, all epilogue warps on the first half and then on the second,
+ *                          and hand each half's accumulator columns back as soon as it is read:
+ *                          the next tile's MMAs on the first half then overlap the drain of the
+ *                          second. A bit mask of FLCE_ROLE_*; -1 restores the default,
+ *                          FLCE_ROLE_FORWARD | FLCE_ROLE_DZ (the roles with K = H).
  *   FLCE_TUNE_CHUNK_BYTES  bytes of bf16 chunk logits the single call (flce_forward_backward)
  *                          may hold at once: it takes as few token chunks of (nearly) equal size
  *                          as this budget and the half-of-all-tokens limit allow. Fewer chunks
@@ -244,6 +251,7 @@ int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_RO
 #define FLCE_TUNE_RASTER_VOCAB 4
 #define FLCE_TUNE_SPLIT_EPILOGUE 5
 #define FLCE_TUNE_CHUNK_BYTES 6
+#define FLCE_TUNE_ORDERED_DRAIN 7
 #define FLCE_ROLE_FORWARD 1
 #define FLCE_ROLE_DZ 2
 #define FLCE_ROLE_GRADS 4

@@ -21,7 +21,7 @@ __all__ = [
     "flce_forward_backward", "flce_forward_backward_workspace_size",
     "flce_forward_backward_chunk_tokens", "flce_test_withhold_signal",
     "flce_version", "flce_timing_enable", "flce_timing_read", "TIMING_ROLES",
-    "flce_set_tuning", "flce_get_tuning", "FLCE_TUNE_RASTER_ROWS", "FLCE_TUNE_SM_PAIRS", "FLCE_TUNE_WIDE_TILES", "FLCE_TUNE_RASTER_VOCAB", "FLCE_TUNE_SPLIT_EPILOGUE", "FLCE_TUNE_CHUNK_BYTES", "FLCE_ROLE_FORWARD", "FLCE_ROLE_DZ", "FLCE_ROLE_GRADS",
+    "flce_set_tuning", "flce_get_tuning", "FLCE_TUNE_RASTER_ROWS", "FLCE_TUNE_SM_PAIRS", "FLCE_TUNE_WIDE_TILES", "FLCE_TUNE_RASTER_VOCAB", "FLCE_TUNE_SPLIT_EPILOGUE", "FLCE_TUNE_CHUNK_BYTES", "FLCE_TUNE_ORDERED_DRAIN", "FLCE_ROLE_FORWARD", "FLCE_ROLE_DZ", "FLCE_ROLE_GRADS",
     "dtype_code", "reduction_code",
 ]
 
@@ -160,6 +160,7 @@ FLCE_TUNE_WIDE_TILES = 3
 FLCE_TUNE_RASTER_VOCAB = 4
 FLCE_TUNE_SPLIT_EPILOGUE = 5
 FLCE_TUNE_CHUNK_BYTES = 6
+FLCE_TUNE_ORDERED_DRAIN = 7
 FLCE_ROLE_FORWARD = 1
 FLCE_ROLE_DZ = 2
 FLCE_ROLE_GRADS = 4

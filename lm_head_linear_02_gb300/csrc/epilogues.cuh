@@ -109,6 +109,16 @@ __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
   lo = x - hi;
 }
 
+// Maximum of 32 values in 16 three-input max instructions (exact: any order gives the same).
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+  float t[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) t[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  t[10] = fmaxf(v[30], v[31]);
+  return max3(max3(t[0], t[1], t[2]), max3(t[3], t[4], t[5]),
+              max3(max3(t[6], t[7], t[8]), t[9], t[10]));
+}
+
 // ------------------------------------------------------------------------------- forward
 // "[example] fused_linear_cross_entropy kernel" (Helion PR #1268), forward: a tiled matmul
 // feeding an online softmax that yields the log-sum-exp and the target logit of each row.
@@ -133,6 +143,10 @@ struct FwdEpi {
   };
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
+  static __device__ __forceinline__ void fetch(const Args& a, int mb, int row, EpiRows& r) {
+    const int t = mb * kBM + row;
+    r.y = t < a.T ? static_cast<long long>(a.target[t]) : -1ll;
+  }
 
   // Fold chunks [c_begin, c_end) of the tile into (m, s); picks up the target logit. With
   // kExclude the target column's term is left out of s (the row's other columns are summed in
@@ -160,31 +174,27 @@ struct FwdEpi {
         for (int j = 0; j < 32; ++j)
           if (j == q) zy = v[j];
       }
-      float cm0 = v[0], cm1 = v[1];
-#pragma unroll
-      for (int j = 2; j < 32; j += 2) {
-        cm0 = fmaxf(cm0, v[j]);
-        cm1 = fmaxf(cm1, v[j + 1]);
-      }
-      const float mn = fmaxf(m, fmaxf(cm0, cm1));
+      const float mn = fmaxf(m, max32(v));
       const float mnl = mn * kLog2e;
+      // four running sums (terms j, j+1, j+2, j+3 of each group of four), kept as two lane pairs
       float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; j += 4) {
-        float e0 = ex2(fmaf(v[j + 0], kLog2e, -mnl));
-        float e1 = ex2(fmaf(v[j + 1], kLog2e, -mnl));
-        float e2 = ex2(fmaf(v[j + 2], kLog2e, -mnl));
-        float e3 = ex2(fmaf(v[j + 3], kLog2e, -mnl));
+        float e0, e1, e2, e3;
+        fma2(e0, e1, v[j + 0], v[j + 1], kLog2e, -mnl);
+        fma2(e2, e3, v[j + 2], v[j + 3], kLog2e, -mnl);
+        e0 = ex2(e0);
+        e1 = ex2(e1);
+        e2 = ex2(e2);
+        e3 = ex2(e3);
         if (kExclude) {
           e0 = j + 0 == q ? 0.f : e0;
           e1 = j + 1 == q ? 0.f : e1;
           e2 = j + 2 == q ? 0.f : e2;
           e3 = j + 3 == q ? 0.f : e3;
         }
-        s0 += e0;
-        s1 += e1;
-        s2 += e2;
-        s3 += e3;
+        add2(s0, s1, e0, e1);
+        add2(s2, s3, e2, e3);
       }
       s = s * ex2((m - mn) * kLog2e) + ((s0 + s1) + (s2 + s3));
       m = mn;
@@ -220,7 +230,7 @@ struct FwdEpi {
     const int t = mb * kBM + ctx.row;
     const bool valid = t < a.T;
     const int n0 = nb * kBN;  // launch-relative column of the tile
-    const long long y = valid ? static_cast<long long>(a.target[t]) - a.col0 : -1ll;
+    const long long y = valid ? ctx.rows.y - a.col0 : -1ll;
     const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
     constexpr int kHalfChunks = kBN / 64;
     float zy = 0.f;
@@ -278,6 +288,10 @@ struct LogitsEpi {
   };
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
+  static __device__ __forceinline__ void fetch(const Args& a, int mb, int row, EpiRows& r) {
+    const int t = mb * kBM + row;
+    r.y = t < a.T ? static_cast<long long>(a.target[t]) : -1ll;
+  }
 
   static __device__ __forceinline__ void half(const Args& a, const EpiCtx& ctx, int t, bool valid,
                                               int nb, int rel, int h) {
@@ -291,10 +305,17 @@ struct LogitsEpi {
       float v[32];
       load_chunk(ctx, c, v);
       const int q = rel - c * 32;
+      if (c0 + 32 <= a.V) {  // uniform
+        m = fmaxf(m, max32(v));
+      } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (c0 + j < a.V) m = fmaxf(m, v[j]);
-        if (j == q) zy = v[j];
+        for (int j = 0; j < 32; ++j)
+          if (c0 + j < a.V) m = fmaxf(m, v[j]);
+      }
+      if (q >= 0 && q < 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j == q) zy = v[j];
       }
     }
     const float ml = m * kLog2e;
@@ -307,12 +328,12 @@ struct LogitsEpi {
       load_chunk(ctx, c, v);
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const float e0 = ex2(fmaf(v[j], kLog2e, -ml));
-        const float e1 = ex2(fmaf(v[j + 1], kLog2e, -ml));
-        s0 += (c0 + j < a.V) ? e0 : 0.f;
-        s1 += (c0 + j + 1 < a.V) ? e1 : 0.f;
-        v[j] -= m;
-        v[j + 1] -= m;
+        float e0, e1;
+        fma2(e0, e1, v[j], v[j + 1], kLog2e, -ml);
+        e0 = ex2(e0);
+        e1 = ex2(e1);
+        add2(s0, s1, (c0 + j < a.V) ? e0 : 0.f, (c0 + j + 1 < a.V) ? e1 : 0.f);
+        fma2(v[j], v[j + 1], v[j], v[j + 1], 1.0f, -m);  // v - m, rounded once
       }
       store_rows_bf16x32(ctx.stage, v, ctx.row & 31, a.zbuf + c0, a.ldz, t - (ctx.row & 31),
                          a.T);
@@ -354,7 +375,7 @@ struct LogitsEpi {
     const int t = mb * kBM + ctx.row;
     const bool valid = t < a.T;
     const int n0 = nb * kBN;
-    const long long y = valid ? static_cast<long long>(a.target[t]) : -1ll;
+    const long long y = valid ? ctx.rows.y : -1ll;
     const int rel = (y >= n0 && y < n0 + kBN) ? static_cast<int>(y - n0) : -1;
     if (ctx.split == 1) {
       half(a, ctx, t, valid, nb, rel, 0);
@@ -389,6 +410,13 @@ struct DzEpi {
   };
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
+  static __device__ __forceinline__ void fetch(const Args& a, int mb, int row, EpiRows& r) {
+    const int t = mb * kBM + row;
+    const bool valid = t < a.T;
+    r.y = valid ? static_cast<long long>(__ldg(a.target + t)) : -1ll;
+    r.lse = valid ? __ldg(a.lse + t) : 0.f;
+    r.scale = (valid && a.row_scale) ? __ldg(a.row_scale + t) : 1.0f;
+  }
 
   static __device__ __forceinline__ void tile(const Args& a, State&, int mb, int nb,
                                               const EpiCtx& ctx) {
@@ -396,9 +424,9 @@ struct DzEpi {
     uint4* stage = ctx.stage;
     const int t = mb * kBM + row;
     const bool valid = t < a.T;
-    const float lsel = valid ? __ldg(a.lse + t) * kLog2e : 0.f;
-    const long long y = valid ? static_cast<long long>(__ldg(a.target + t)) : -1ll;
-    const float rs = (valid && a.row_scale) ? __ldg(a.row_scale + t) : 1.0f;
+    const float lsel = ctx.rows.lse * kLog2e;
+    const long long y = ctx.rows.y;
+    const float rs = ctx.rows.scale;
     const int n0 = nb * kBN;  // slab-relative column of the tile
     const long long rel = y - a.slab0 - n0;
     const bool unit_scale = a.row_scale == nullptr;  // uniform: sum / mean reductions
@@ -412,7 +440,11 @@ struct DzEpi {
         // The common case: every column inside the slab and row factor 1, so only the one
         // target column of a row (if it lies in this chunk) differs from exp(z - lse).
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = ex2(fmaf(v[j], kLog2e, -lsel));
+        for (int j = 0; j < 32; j += 2) {
+          fma2(v[j], v[j + 1], v[j], v[j + 1], kLog2e, -lsel);
+          v[j] = ex2(v[j]);
+          v[j + 1] = ex2(v[j + 1]);
+        }
         const long long q = rel - c * 32;
         if (q >= 0 && q < 32) {
 #pragma unroll
@@ -472,6 +504,7 @@ struct GradWEpi {
   static __device__ __forceinline__ void init(const Args& a, State& st) {
     st.g = a.grad_loss ? __ldg(a.grad_loss) * a.scale : a.scale;
   }
+  static __device__ __forceinline__ void fetch(const Args&, int, int, EpiRows&) {}
 
   static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb,
                                               const EpiCtx& ctx) {
@@ -543,6 +576,7 @@ struct GradXEpi {
   static __device__ __forceinline__ void init(const Args& a, State& st) {
     st.g = a.grad_loss ? __ldg(a.grad_loss) * a.scale : a.scale;
   }
+  static __device__ __forceinline__ void fetch(const Args&, int, int, EpiRows&) {}
 
   static __device__ __forceinline__ void tile(const Args& a, State& st, int mb, int nb,
                                               const EpiCtx& ctx) {

@@ -79,6 +79,7 @@ namespace {
 std::atomic<int> g_tune_raster_rows{2048};
 std::atomic<int> g_tune_raster_vocab{kDefaultRasterVocab};
 std::atomic<int> g_tune_split_epilogue{kDefaultSplitEpilogue};
+std::atomic<int> g_tune_ordered_drain{kDefaultOrderedDrain};
 std::atomic<int> g_tune_sm_pairs{-1};
 std::atomic<int> g_tune_wide_tiles{-1};
 }  // namespace
@@ -86,6 +87,7 @@ std::atomic<int> g_tune_wide_tiles{-1};
 int tune_raster_rows() { return g_tune_raster_rows.load(); }
 int tune_raster_vocab() { return g_tune_raster_vocab.load(); }
 int tune_split_epilogue() { return g_tune_split_epilogue.load(); }
+int tune_ordered_drain() { return g_tune_ordered_drain.load(); }
 
 namespace {
 std::atomic<int> g_withhold_request{0};
@@ -468,6 +470,11 @@ int flce_set_tuning(int key, int64_t value) {
       flce::g_tune_split_epilogue.store(value < 0 ? flce::kDefaultSplitEpilogue
                                                   : static_cast<int>(value));
       return FLCE_OK;
+    case FLCE_TUNE_ORDERED_DRAIN:
+      if (value < -1 || value > 7) return FLCE_ERR_ARG;
+      flce::g_tune_ordered_drain.store(value < 0 ? flce::kDefaultOrderedDrain
+                                                 : static_cast<int>(value));
+      return FLCE_OK;
     case FLCE_TUNE_WIDE_TILES:
       if (value < -1 || value > 7) return FLCE_ERR_ARG;
       flce::g_tune_wide_tiles.store(static_cast<int>(value));
@@ -491,6 +498,9 @@ int flce_get_tuning(int key, int64_t* value) {
       return FLCE_OK;
     case FLCE_TUNE_CHUNK_BYTES:
       *value = g_chunk_bytes.load();
+      return FLCE_OK;
+    case FLCE_TUNE_ORDERED_DRAIN:
+      *value = flce::g_tune_ordered_drain.load();
       return FLCE_OK;
     case FLCE_TUNE_SM_PAIRS: {
       flce::Device dev;

@@ -84,7 +84,8 @@ cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
     g.p[1].tile_begin = x.m_tiles * x.n_tiles;
     if (core != kCoreSingle)
       return launch_pair_core<GradXEpi<false>, GradWEpi<false>>(core, tdz_k, tw_mn, tdz_mn, tx_mn,
-                                                                g, ex, ew, pw.sms, pw.stream);
+                                                                g, ex, ew, pw.sms, pw.stream,
+                                                                FLCE_ROLE_GRADS);
     return launch_gemm<false, GradXEpi<false>, GradWEpi<false>>(tdz_k, tw_mn, tdz_mn, tx_mn, g, ex,
                                                                 ew, pw.sms, pw.stream);
   }
@@ -93,7 +94,8 @@ cudaError_t launch_grads_bf16(const CUtensorMap& tdz_mn, const CUtensorMap& tx_m
   g.p[1].tile_begin = w.m_tiles * w.n_tiles;
   if (core != kCoreSingle)
     return launch_pair_core<GradWEpi<false>, GradXEpi<false>>(core, tdz_mn, tx_mn, tdz_k, tw_mn, g,
-                                                              ew, ex, pw.sms, pw.stream);
+                                                              ew, ex, pw.sms, pw.stream,
+                                                              FLCE_ROLE_GRADS);
   return launch_gemm<false, GradWEpi<false>, GradXEpi<false>>(tdz_mn, tx_mn, tdz_k, tw_mn, g, ew,
                                                               ex, pw.sms, pw.stream);
 }

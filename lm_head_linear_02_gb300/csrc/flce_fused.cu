@@ -105,7 +105,8 @@ cudaError_t launch_chunk_grads(const CUtensorMap& tz_k, const CUtensorMap& tw_mn
   g.tile_counter = c.tile_counter;
   if (core != kCoreSingle)
     return launch_pair_core<GradXEpi<false>, GradXEpi<false>>(core, tz_k, tw_mn, tz_mn, tx_mn, g, ex,
-                                                              ew, c.sms, c.stream);
+                                                              ew, c.sms, c.stream,
+                                                              FLCE_ROLE_GRADS);
   return launch_gemm<false, GradXEpi<false>, GradXEpi<false>>(tz_k, tw_mn, tz_mn, tx_mn, g, ex, ew,
                                                               c.sms, c.stream);
 }

@@ -32,6 +32,10 @@ constexpr int kTileN = 256;
 int tune_raster_rows();
 int tune_raster_vocab();
 int tune_split_epilogue();
+//   tune_ordered_drain(): bit mask of the roles whose wide pair tiles (one epilogue warp per row
+//                       block) drain their two 128-row halves one after the other, so that the
+//                       next tile's MMAs on the first half overlap the drain of the second.
+int tune_ordered_drain();
 int tune_sm_pairs();
 int tune_wide_tiles();
 
@@ -57,6 +61,14 @@ constexpr int64_t kDefaultChunkBytes = int64_t(3) << 29;
 // Llama-2 head: two epilogue warps per row block left the tensor pipe's active cycles where
 // they were (dz 85.8% -> 85.2%, forward 89.3% -> 89.4%) and the launches 0.3% slower.
 constexpr int kDefaultSplitEpilogue = 0;
+
+// Default of tune_ordered_drain(): the forward projection (and the single call's chunk logits)
+// and dz, whose K = H main loops are short enough for the drain to matter. Measured on GB300
+// at T = 16384, H = 4096, V = 128256 against draining both halves together: a tile's period
+// (SM clock stamps per tile) 1.4% shorter for the forward and 2.3% for dz; in the power-capped
+// step the forward launch 0.6% and dz 1.4% faster, the step 0.3-0.5%. The gradient launch,
+// whose tiles run K = 16384 or 32256, has nothing to gain.
+constexpr int kDefaultOrderedDrain = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ;
 
 // Roles measured faster on 256-row CTA tiles when they run on CTA pairs.
 constexpr int kDefaultWideRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ | FLCE_ROLE_GRADS;

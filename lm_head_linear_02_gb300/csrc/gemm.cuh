@@ -63,6 +63,8 @@ struct GemmGrid {
   int* tile_counter;  // null: CTA b takes tiles b, b + grid, ...; else a zeroed device int that
                       // hands out tiles in list order to whichever CTA is free (dynamic)
   int withhold;       // testing aid: CTA 0 (pair 0) does not signal its first accumulator tile
+  int ordered;        // wide pair tiles only: drain the two 128-row halves one after the other
+                      // (see k_umma_gemm_pair); 0 on every other core
 };
 
 // Depth of the per-CTA queue through which the producer hands tile indices to the MMA thread
@@ -132,6 +134,15 @@ struct StageGeom {
 // 32 float4 slots, alternating with `iter`, the warp's tile count) and the mbarrier xbar (32
 // arrivals per tile, phase parity iter & 1): part 1 writes and arrives, part 0 waits, bounded
 // like every pipeline wait, so a partner that left on the abort path cannot hang it.
+// Per-row inputs of an epilogue (target id, log-sum-exp, upstream factor of this thread's row),
+// loaded by Epi::fetch as soon as the tile index is known, while the accumulator is still being
+// computed, so that their global-memory latency is not paid after the tile is finished.
+struct EpiRows {
+  long long y;
+  float lse;
+  float scale;
+};
+
 struct EpiCtx {
   int row;            // accumulator row of this thread within the 128-row block
   uint32_t taddr;     // TMEM address of this warp's lane quarter, column 0 of the block
@@ -145,12 +156,14 @@ struct EpiCtx {
   float4* xchg;       // exchange slots of those two warps (split 2)
   int* status;        // device status word (a timed-out exchange sets FLCE_STATUS_TIMEOUT)
   volatile int* abort;
+  EpiRows rows;       // this row's inputs (Epi::fetch with the same 128-row block index)
 };
 
 struct NoEpi {
   struct Args {};
   struct State {};
   static __device__ __forceinline__ void init(const Args&, State&) {}
+  static __device__ __forceinline__ void fetch(const Args&, int, int, EpiRows&) {}
   static __device__ __forceinline__ void tile(const Args&, State&, int, int, const EpiCtx&) {}
 };
 
@@ -394,10 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         qphase ^= 1u;
       }
       if (t < 0) break;
+      const TileInfo ti = map_tile(g, t);
+      EpiRows rows;
+      if (ti.prob == 0)
+        Epi0::fetch(e0, ti.mb, row, rows);
+      else
+        Epi1::fetch(e1, ti.mb, row, rows);
       if (!mbar_wait(tfull_bar(acc), acc_phase, g.status, abort_flag)) break;
       tc_fence_after_sync();
       __syncwarp();
-      const TileInfo ti = map_tile(g, t);
       EpiCtx ctx;
       ctx.row = row;
       ctx.taddr =
@@ -414,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ctx.xchg = nullptr;
       ctx.status = g.status;
       ctx.abort = abort_flag;
+      ctx.rows = rows;
       if (ti.prob == 0)
         Epi0::tile(e0, st0, ti.mb, ti.nb, ctx);
       else

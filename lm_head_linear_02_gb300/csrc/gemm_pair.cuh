@@ -13,7 +13,9 @@
 //                TMA fill rate of one SM, not the tensor core, bounds the 128-row geometry (about
 //                40-50 B per SM clock measured, 64 needed), so this one keeps the tensor pipe
 //                busy; the price is one accumulator filling all 512 TMEM columns, so the epilogue
-//                of a tile is not hidden behind the next main loop (8 epilogue warps halve it).
+//                of a tile is only partly hidden: with the ordered drain (g.ordered) the 8
+//                epilogue warps read the first 128-row half, hand its columns back, and the next
+//                tile's MMAs on that half run while they read the second.
 //
 // Roles (per CTA: 2 + 4 (kRows / 128) kSplit warps):
 //   warp 0 (both CTAs)   TMA producer: loads this CTA's A rows and B half; completion is counted
@@ -25,7 +27,13 @@
 //                        (q' = warp % 4, the lane quarter a warp may access), then tells the
 //                        leader (remote mbarrier arrive) that the accumulator is free. With
 //                        kSplit = 2 a second set of warps (2 + 4 kHalves + ...) takes columns
-//                        128-255 of the same rows and the first set columns 0-127.
+//                        128-255 of the same rows and the first set columns 0-127. Ordered
+//                        drain (wide tiles, kSplit = 1): warp 2 + 4p + q takes columns
+//                        [128p, 128p + 128) of lane quarter q' in half 0, then in half 1, and
+//                        releases each half on its own barrier (tmem_empty 0 and 1).
+// Each epilogue warp loads its rows' inputs (Epi::fetch) as soon as it knows the next tile,
+// before the accumulator is ready, and releases TMEM with a CTA-scope arrive, which does not
+// wait for the tile's global stores to become visible to the cluster.
 // A launch may carry two independent problems: grad_W and grad_x of one vocab slab run together,
 // so that their tiles fill the GPU in one wave pattern instead of two.
 #pragma once
@@ -67,6 +75,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
                      const __grid_constant__ CUtensorMap tB1, const GemmGrid g,
                      const typename Epi0::Args e0, const typename Epi1::Args e1) {
   using G = PairGeom<kRows, kSplit>;
+  // wide tiles with one warp per (lane quarter, column half) may drain their halves in order
+  constexpr bool kOrderable = G::kHalves == 2 && kSplit == 1;
   constexpr int kPairStages = G::kStages;
   constexpr uint32_t kPairABytes = G::kABytes;
   constexpr uint32_t kPairStageBytes = G::kStageBytes;
@@ -257,26 +267,79 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
         if (!mbar_wait_cluster(tempty_bar(acc), acc_phase ^ 1u, g.status, abort_flag)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * G::kHalves * kBN);
-        for (int kb = 0; kb < k_blocks; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, g.status, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint64_t soff = static_cast<uint64_t>(stage * kPairStageBytes) >> 4;
+        // The MMAs of one 128-row half over the 64-deep K slice in ring stage s.
+        auto issue_half = [&](int s, int h, int kb) {
+          const uint64_t soff = static_cast<uint64_t>(s * kPairStageBytes) >> 4;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-            for (int h = 0; h < G::kHalves; ++h)  // half h: A rows [128h, 128h + 128), +16 KB
-              mma_bf16_pair(d_tmem + static_cast<uint32_t>(h * kBN),
-                            a_base + soff + h * (16384u >> 4) + kk * a_step,
-                            b_base + soff + kk * b_step, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)  // half h: A rows [128h, 128h + 128), +16 KB
+            mma_bf16_pair(d_tmem + static_cast<uint32_t>(h * kBN),
+                          a_base + soff + h * (16384u >> 4) + kk * a_step,
+                          b_base + soff + kk * b_step, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+        };
+        if (kOrderable && g.ordered) {
+          // Ordered drain (the epilogue releases half 0's TMEM columns, then half 1's): the
+          // tile starts on half 0 alone, and half 1's MMAs trail by the stages filled before
+          // half 1 was released (at most the ring's depth), so the tensor pipe works through
+          // the second half of the previous tile's epilogue. Each stage is released once both
+          // halves have used it. Every accumulator element still sums its K slices in order.
+          bool h1_free = false;
+          int lag = 0;            // first K block whose half-1 MMAs are not issued yet
+          int lag_stage = stage;  // its ring stage
+          for (int kb = 0; kb < k_blocks; ++kb) {
+            if (!mbar_wait(full_bar(stage), phase, g.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_half(stage, 0, kb);
+            if (!h1_free) {
+              if (kb + 1 - lag == kPairStages || kb + 1 == k_blocks) {
+                // every stage waits for half 1, or the tile ends: wait for the release
+                if (!mbar_wait_cluster(tempty_bar(1), acc_phase ^ 1u, g.status, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                h1_free = true;
+              } else {
+                h1_free = mbar_test_cluster(tempty_bar(1), acc_phase ^ 1u) != 0;
+              }
+              if (h1_free) tc_fence_after_sync();
+            }
+            if (h1_free) {
+              for (; lag <= kb; ++lag) {
+                issue_half(lag_stage, 1, lag);
+                mma_commit_pair(empty_bar(lag_stage), 0x3);
+                ++consumed;
+                if (++lag_stage == kPairStages) lag_stage = 0;
+              }
+            }
+            if (++stage == kPairStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          mma_commit_pair(empty_bar(stage), 0x3);
-          ++consumed;
-          if (++stage == kPairStages) {
-            stage = 0;
-            phase ^= 1u;
+        } else {
+          for (int kb = 0; kb < k_blocks; ++kb) {
+            if (!mbar_wait(full_bar(stage), phase, g.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint64_t soff = static_cast<uint64_t>(stage * kPairStageBytes) >> 4;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+              for (int h = 0; h < G::kHalves; ++h)
+                mma_bf16_pair(d_tmem + static_cast<uint32_t>(h * kBN),
+                              a_base + soff + h * (16384u >> 4) + kk * a_step,
+                              b_base + soff + kk * b_step, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit_pair(empty_bar(stage), 0x3);
+            ++consumed;
+            if (++stage == kPairStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
         if (!ok) break;
@@ -308,6 +371,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
     const int e_part0 = 4 * half + ((quarter - 2) & 3);
     float4* xchg = reinterpret_cast<float4*>(smem + kPairRingBytes + 1024 +
                                              static_cast<uint32_t>(e_part0) * kEpiStageBytes);
+    // ordered drain: warp 2 + 4 p + (q - 2) % 4 takes column half p of lane quarter q in both
+    // row halves; the part-0 warp lends its staging as 2 halves x 2 slots of 32 float4 (2 KB)
+    float4* xchg_ordered = reinterpret_cast<float4*>(
+        smem + kPairRingBytes + 1024 + static_cast<uint32_t>((quarter - 2) & 3) * kEpiStageBytes);
+    static_assert(kEpiStageBytes >= 2 * 2 * 32 * sizeof(float4), "ordered-drain exchange slots");
     int acc = 0;
     uint32_t acc_phase = 0;
     typename Epi0::State st0;
@@ -327,34 +395,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
         qphase ^= 1u;
       }
       if (t < 0) break;
+      const TileInfo pt = map_tile(g, t);
+      // Ordered drain: the 8 warps take column half `grp` of both 128-row halves, half 0
+      // first, and release each half's TMEM columns as soon as it is drained (tempty_bar(h)),
+      // so that the next tile's half-0 MMAs overlap the drain of half 1. Otherwise each warp
+      // drains its own half and columns once and releases the accumulator (tempty_bar(acc)).
+      const bool ordered = kOrderable && g.ordered;  // uniform
+      const int n_pass = ordered ? 2 : 1;
+      const int mb_first =
+          (pt.mb * 2 + static_cast<int>(rank)) * G::kHalves + (ordered ? 0 : half);
+      EpiRows rows0, rows1;  // the rows' inputs, loaded while the MMAs still run
+      if (pt.prob == 0)
+        Epi0::fetch(e0, mb_first, row, rows0);
+      else
+        Epi1::fetch(e1, mb_first, row, rows0);
+      rows1 = rows0;
+      if (ordered) {
+        if (pt.prob == 0)
+          Epi0::fetch(e0, mb_first + 1, row, rows1);
+        else
+          Epi1::fetch(e1, mb_first + 1, row, rows1);
+      }
       if (!mbar_wait(tfull_bar(acc), acc_phase, g.status, abort_flag)) break;
       tc_fence_after_sync();
       __syncwarp();
-      const TileInfo pt = map_tile(g, t);
-      const int mb128 = (pt.mb * 2 + static_cast<int>(rank)) * G::kHalves + half;
-      EpiCtx ctx;
-      ctx.row = row;
-      ctx.taddr = tmem_base + static_cast<uint32_t>((acc * G::kHalves + half) * kBN) +
-                  (static_cast<uint32_t>(quarter * 32) << 16);
-      ctx.stage = stage;
-      ctx.c_begin = part * (kBN / 32 / kSplit);
-      ctx.c_end = ctx.c_begin + kBN / 32 / kSplit;
-      ctx.part = part;
-      ctx.split = kSplit;
-      ctx.iter = iter++;
-      ctx.two_acc = 0;
-      ctx.taddr_corr = 0;
-      ctx.xbar = x_bar(quarter + 4 * half);
-      ctx.xchg = xchg;
-      ctx.status = g.status;
-      ctx.abort = abort_flag;
-      if (pt.prob == 0)
-        Epi0::tile(e0, st0, mb128, pt.nb, ctx);
-      else
-        Epi1::tile(e1, st1, mb128, pt.nb, ctx);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+#pragma unroll 1
+      for (int pass = 0; pass < n_pass; ++pass) {
+        const int h = ordered ? pass : half;
+        const int col_part = ordered ? grp : part;
+        const int mb128 = mb_first + pass;
+        EpiCtx ctx;
+        ctx.row = row;
+        ctx.taddr = tmem_base + static_cast<uint32_t>((acc * G::kHalves + h) * kBN) +
+                    (static_cast<uint32_t>(quarter * 32) << 16);
+        ctx.stage = stage;
+        ctx.split = ordered ? 2 : kSplit;
+        ctx.c_begin = col_part * (kBN / 32 / ctx.split);
+        ctx.c_end = ctx.c_begin + kBN / 32 / ctx.split;
+        ctx.part = col_part;
+        ctx.iter = iter;
+        ctx.two_acc = 0;
+        ctx.taddr_corr = 0;
+        ctx.xbar = x_bar(quarter + 4 * h);
+        ctx.xchg = ordered ? xchg_ordered + 64 * h : xchg;
+        ctx.status = g.status;
+        ctx.abort = abort_flag;
+        ctx.rows = pass == 0 ? rows0 : rows1;
+        if (pt.prob == 0)
+          Epi0::tile(e0, st0, mb128, pt.nb, ctx);
+        else
+          Epi1::tile(e1, st1, mb128, pt.nb, ctx);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_cta(mapa_shared(tempty_bar(ordered ? h : acc), 0));
+      }
+      ++iter;
       if (++acc == G::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
@@ -445,15 +540,18 @@ cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& b0, const CUte
 // Launch on a pair core (kCorePair: 128-row CTA tiles, kCoreWide: 256-row CTA tiles); the
 // problems must have been made with core_tile_rows(core). kSplitWide: epilogue warps per row
 // block on the wide core (2 for roles whose epilogues fit the smaller register budget of 576
-// threads, when `role` is in the tune_split_epilogue() mask).
+// threads, when `role` is in the tune_split_epilogue() mask). Otherwise wide tiles of a role in
+// the tune_ordered_drain() mask drain their two row halves one after the other.
 template <class Epi0, class Epi1, int kSplitWide = 1>
 cudaError_t launch_pair_core(Core core, const CUtensorMap& a0, const CUtensorMap& b0,
                              const CUtensorMap& a1, const CUtensorMap& b1, GemmGrid g,
                              const typename Epi0::Args& e0, const typename Epi1::Args& e1, int sms,
                              cudaStream_t stream, int role = 0) {
+  g.ordered = 0;
   if (core == kCoreWide) {
     if (kSplitWide == 2 && (tune_split_epilogue() & role) != 0)
       return launch_pair<256, kSplitWide, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
+    g.ordered = (tune_ordered_drain() & role) != 0 ? 1 : 0;
     return launch_pair<256, 1, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
   }
   return launch_pair<128, 1, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);

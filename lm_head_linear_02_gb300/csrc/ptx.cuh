@@ -253,6 +253,19 @@ __device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint32_t bar, uint32_t
   return done;
 }
 
+// One non-blocking look (cluster-scope acquire): has the phase with the given parity completed?
+__device__ __forceinline__ uint32_t mbar_test_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done;
+}
+
 // Bounded wait with cluster-scope acquire (arrivals come from the peer CTA's threads).
 __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* status,
                                                   volatile int* abort) {
@@ -332,6 +345,47 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Two-lane fp32 arithmetic (Blackwell's packed .f32x2 forms): one instruction for two
+// independent lanes, each rounded exactly like its scalar counterpart (fmaf, +), so code that
+// keeps its chains lane by lane gets the same bits with half the instructions.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 A, B, C, D;\n\t"
+      "mov.b64 A, {%2, %3};\n\t"
+      "mov.b64 B, {%4, %4};\n\t"
+      "mov.b64 C, {%5, %5};\n\t"
+      "fma.rn.f32x2 D, A, B, C;\n\t"
+      "mov.b64 {%0, %1}, D;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1), lane by lane.
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 S, A;\n\t"
+      "mov.b64 S, {%0, %1};\n\t"
+      "mov.b64 A, {%2, %3};\n\t"
+      "add.rn.f32x2 S, S, A;\n\t"
+      "mov.b64 {%0, %1}, S;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
+// max(a, b, c) in one instruction; exact, like fmaxf(a, fmaxf(b, c)) for non-NaN inputs.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (cluster-window address) with release at
+// CTA scope only: it orders this thread's earlier tcgen05 reads (completed by tcgen05.wait::ld
+// and fenced by tcgen05.fence::before_thread_sync) before the arrival without waiting for its
+// earlier global stores to become visible cluster-wide, which the barrier does not publish.
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -195,7 +195,8 @@ def test_tuning_knobs_validate(lib):
                      (B.FLCE_TUNE_WIDE_TILES, 8), (B.FLCE_TUNE_WIDE_TILES, -2),
                      (B.FLCE_TUNE_RASTER_VOCAB, 100), (B.FLCE_TUNE_RASTER_VOCAB, -256),
                      (B.FLCE_TUNE_SPLIT_EPILOGUE, 8), (B.FLCE_TUNE_SPLIT_EPILOGUE, -2),
-                     (B.FLCE_TUNE_CHUNK_BYTES, -1), (99, 1)]:
+                     (B.FLCE_TUNE_CHUNK_BYTES, -1), (B.FLCE_TUNE_ORDERED_DRAIN, 8),
+                     (B.FLCE_TUNE_ORDERED_DRAIN, -2), (99, 1)]:
         with pytest.raises(B.FlceError):
             B.flce_set_tuning(key, bad)
     B.flce_set_tuning(B.FLCE_TUNE_RASTER_ROWS, 4096)
@@ -226,6 +227,15 @@ def test_tuning_knobs_validate(lib):
     finally:
         B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
     assert B.flce_get_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE) == 0
+    # row halves drained one after the other: a role mask; -1 restores the default
+    default = B.flce_get_tuning(B.FLCE_TUNE_ORDERED_DRAIN)
+    assert default == B.FLCE_ROLE_FORWARD | B.FLCE_ROLE_DZ
+    B.flce_set_tuning(B.FLCE_TUNE_ORDERED_DRAIN, B.FLCE_ROLE_DZ)
+    try:
+        assert B.flce_get_tuning(B.FLCE_TUNE_ORDERED_DRAIN) == B.FLCE_ROLE_DZ
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_ORDERED_DRAIN, -1)
+    assert B.flce_get_tuning(B.FLCE_TUNE_ORDERED_DRAIN) == default
 
 
 def test_single_call_chunk_rule(lib):

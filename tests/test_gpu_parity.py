@@ -162,19 +162,23 @@ def test_parity_single_sm_and_sm_pair_tiles(pair, wide):
 
 def test_contraction_cores_agree():
     """The three contraction cores (single-SM, SM pairs with 128-row and with 256-row CTA tiles,
-    the last with one or two epilogue warps per row block, and in either raster order) sum
-    every output element over K in the same order and form every per-row partial the same
-    way, so all outputs agree bit for bit, for both schedules."""
+    the last with one or two epilogue warps per row block, its two row halves drained together
+    or one after the other, and in either raster order) sum every output element over K in the
+    same order and form every per-row partial the same way, so all outputs agree bit for bit,
+    for both schedules."""
     inp = make_inputs("tiny", T=1100, H=320, V=3000, dtype="bf16", seed=33)
     x, w, y = to_device(inp)
     outs, fused = [], []
     try:
-        for pair, wide, split, rv in [(0, 0, -1, 4096), (7, 0, -1, 4096), (7, 7, -1, 4096),
-                                      (7, 7, 3, 4096), (7, 7, -1, 0), (7, 7, -1, 1024)]:
+        for pair, wide, split, rv, ordered in [
+                (0, 0, -1, 4096, 0), (7, 0, -1, 4096, 0), (7, 7, -1, 4096, 0),
+                (7, 7, 3, 4096, 0), (7, 7, -1, 0, 0), (7, 7, -1, 1024, 0),
+                (7, 7, -1, 4096, 7), (7, 7, -1, 0, 7), (7, 7, 3, 4096, 4)]:
             B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
             B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
             B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, split)
             B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, rv)
+            B.flce_set_tuning(B.FLCE_TUNE_ORDERED_DRAIN, ordered)
             loss, lse, status = A.flce_forward(x, w, y, "mean")
             gx, gw, status_b = A.flce_backward(x, w, y, lse, torch.ones((), device="cuda"), "mean")
             torch.cuda.synchronize()
@@ -188,6 +192,7 @@ def test_contraction_cores_agree():
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
         B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
         B.flce_set_tuning(B.FLCE_TUNE_RASTER_VOCAB, 4096)
+        B.flce_set_tuning(B.FLCE_TUNE_ORDERED_DRAIN, -1)
     for other in outs[1:]:
         for a, b in zip(outs[0], other):
             assert np.array_equal(a, b)
@@ -291,12 +296,13 @@ def test_out_of_range_target_sets_status_and_nan_loss():
         A.check_status(status)
 
 
-@pytest.mark.parametrize("pair,wide,split", [(0, 0, -1), (7, 0, -1), (7, 7, -1), (7, 7, 3)])
-def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide, split):
+@pytest.mark.parametrize("pair,wide,split,ordered", [(0, 0, -1, 0), (7, 0, -1, 0), (7, 7, -1, 0),
+                                                     (7, 7, 3, 0), (7, 7, -1, 7)])
+def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide, split, ordered):
     """A withheld pipeline signal ends the launch with FLCE_STATUS_TIMEOUT after the bounded wait
     (about 2 s) instead of hanging, on each contraction core (single SM, SM pairs with 128-row
-    and with 256-row CTA tiles, whose abort path also drains the partner CTA); the next calls
-    run normally on the same context."""
+    and with 256-row CTA tiles, whose abort path also drains the partner CTA, and the latter
+    with its row halves drained in order); the next calls run normally on the same context."""
     import time
 
     inp = make_inputs("ragged", dtype="bf16")
@@ -304,6 +310,7 @@ def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide, split)
     B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
     B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
     B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, split)
+    B.flce_set_tuning(B.FLCE_TUNE_ORDERED_DRAIN, ordered)
     try:
         B.flce_test_withhold_signal()
         t0 = time.time()
@@ -318,7 +325,9 @@ def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide, split)
         B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
         B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, -1)
         B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
-    assert_full_parity(inp, "mean", label=f"after timeout pair={pair} wide={wide} split={split}")
+        B.flce_set_tuning(B.FLCE_TUNE_ORDERED_DRAIN, -1)
+    assert_full_parity(inp, "mean", label=f"after timeout pair={pair} wide={wide} split={split} "
+                       f"ordered={ordered}")
 
 
 def test_sum_mean_and_grad_loss_scaling():
