@@ -14,6 +14,8 @@
 //                one launch, dynamic tiles; grad_W is written by the first chunk and summed in
 //                place, in its bf16 output, by the later ones (in chunk order)
 // FLOPs: 6 T H V (forward + two gradient contractions) instead of 8 T H V with recompute.
+#include <algorithm>
+
 #include "epilogues.cuh"
 #include "flce_internal.h"
 #include "gemm_pair.cuh"
@@ -63,8 +65,14 @@ cudaError_t launch_chunk_logits(const CUtensorMap& tx_c, const CUtensorMap& tw,
   LogitsEpi::Args ea{c.target, c.part_m, c.part_s, c.zy, c.sx, c.zbuf, c.ldz, c.rows, c.V};
   const Core core = role_core(c.sms, FLCE_ROLE_FORWARD);  // maps boxed for this core
   GemmGrid g{};
-  // token-row raster: a chunk's x rows (at most a few thousand) are what stays in L2 here
-  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, core_tile_rows(core), 0, false);
+  // token-row raster: the chunk's x rows stay in L2 while W streams past, in one group when
+  // they fit in kChunkRowsL2Bytes (then each W tile is read from DRAM once per chunk, by the
+  // tiles of all the chunk's rows in the same wave), else in groups of that size
+  const int tile_rows = core_tile_rows(core);
+  g.p[0] = make_problem(c.rows, c.V, c.H, 64, false, false, tile_rows, 0, false);
+  const int64_t tile_x_bytes = static_cast<int64_t>(tile_rows) * c.H * 2;
+  const int fit = static_cast<int>(std::max<int64_t>(1, kChunkRowsL2Bytes / tile_x_bytes));
+  g.p[0].group_m = std::max(g.p[0].group_m, std::min(g.p[0].m_tiles, fit));
   g.num_problems = 1;
   g.status = c.status;
   g.tile_counter = c.tile_counter;  // tiles in list order: the pairs sharing a W tile stay in step

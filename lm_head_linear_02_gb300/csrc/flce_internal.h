@@ -54,6 +54,10 @@ constexpr int kAutoPairRoles = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ | FLCE_ROLE_GRAD
 // streams past) and ran no faster.
 constexpr int kDefaultRasterVocab = 4096;
 
+// Token rows of a single-call chunk kept in L2 as one raster group of its logits launch
+// (46 MB for 5632 rows at H = 4096).
+constexpr int64_t kChunkRowsL2Bytes = int64_t(48) << 20;
+
 // Default bf16 chunk-logits budget of the single call (FLCE_TUNE_CHUNK_BYTES): 1.5 GiB.
 constexpr int64_t kDefaultChunkBytes = int64_t(3) << 29;
 
