@@ -202,6 +202,31 @@ def test_contraction_cores_agree():
             assert np.array_equal(a, b)
 
 
+def test_drain_modes_agree_with_many_tiles_per_pair():
+    """Wide pair tiles drained half by half (the next tile's MMAs on the first half start while
+    the second half is read) or both halves together, or by 16 epilogue warps, give the same
+    bits. 4096 x 1024 x 32000 is 1000 pair tiles, about 13 per pair, so every pair hands its
+    accumulator from one tile to the next many times; the single call (two chunks) too."""
+    inp = make_inputs("tiny", T=4096, H=1024, V=32000, dtype="bf16", seed=41)
+    x, w, y = to_device(inp)
+    outs, fused = [], []
+    try:
+        for ordered, split in [(0, 0), (7, 0), (0, 3)]:
+            B.flce_set_tuning(B.FLCE_TUNE_ORDERED_DRAIN, ordered)
+            B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, split)
+            loss, lse, gx, gw = run_gpu(x, w, y, "mean")
+            outs.append((loss, lse, gx, gw))
+            fused.append(run_fused(x, w, y, "mean", 1.0))
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_ORDERED_DRAIN, -1)
+        B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
+    for runs in (outs, fused):
+        for other in runs[1:]:
+            assert runs[0][0] == other[0]
+            for a, b in zip(runs[0][1:], other[1:]):
+                assert np.array_equal(a, b)
+
+
 @pytest.mark.parametrize("T,H,V,dtype", [
     (1, 64, 7, "bf16"),       # one token, vocab far below one tile
     (1, 8, 1, "f32"),         # V = 1: lse = z, loss 0, zero gradients
