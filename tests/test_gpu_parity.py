@@ -248,6 +248,54 @@ def test_parity_edge_shapes(T, H, V, dtype):
     assert_full_parity(inp, "mean", label=f"edge {T}x{H}x{V} {dtype}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_activations_closed_form(dtype):
+    """x = 0 makes every logit 0: lse = ln V, every per-token loss ln V, grad_W = dz^T x = 0
+    exactly, and grad_x[t] = g (mean_v W[v] - W[y_t]) with g = 1 / T (mean), a closed form
+    independent of the oracle."""
+    inp = make_inputs("tiny", T=300, H=200, V=3000, dtype=dtype, seed=23)
+    inp.x[:] = 0.0
+    if dtype == "bf16":
+        inp.x_bits[:] = 0
+    x, w, y = to_device(inp)
+    loss, lse, gx, gw = run_gpu(x, w, y, "mean")
+    V, T = 3000, 300
+    assert abs(loss - math.log(V)) / math.log(V) <= TOL[dtype]["loss"]
+    assert np.abs(lse - math.log(V)).max() <= 1e-5 * math.log(V)
+    assert np.all(gw == 0.0)
+    W = inp.weight.astype(np.float64)  # the values both paths see (bf16-exact for bf16)
+    expect = (W.mean(axis=0)[None, :] - W[inp.target]) / T
+    assert norm_err(gx, expect) <= TOL[dtype]["grad"]
+
+
+def test_gradient_invariants_bf16():
+    """Every row of dz = softmax - onehot sums to 0, so every column of grad_W sums to 0 over the
+    vocabulary (up to the rounding of the bf16 dz slab and of grad_W itself)."""
+    inp = make_inputs("tiny", T=1024, H=512, V=8000, dtype="bf16", seed=29)
+    x, w, y = to_device(inp)
+    loss, lse, gx, gw = run_gpu(x, w, y, "mean")
+    col = np.abs(gw.sum(axis=0))
+    scale = np.abs(gw).sum(axis=0)
+    assert (col / scale).max() <= 2e-3
+
+
+def test_shift_of_all_weight_rows_f32():
+    """Adding one vector a to every weight row adds x_t . a to every logit of row t: lse moves by
+    x_t . a, while the softmax, the loss and both gradients stay as they were (fp32 inputs, whose
+    shifted weights are exact enough for the fp32 tolerances)."""
+    inp = make_inputs("tiny", T=300, H=200, V=3000, dtype="f32", seed=31)
+    a = np.random.default_rng(5).normal(0.0, 0.02, size=200).astype(np.float32)
+    x, w, y = to_device(inp)
+    l0, lse0, gx0, gw0 = run_gpu(x, w, y, "mean")
+    w1 = torch.from_numpy(inp.weight + a[None, :]).cuda()
+    l1, lse1, gx1, gw1 = run_gpu(x, w1, y, "mean")
+    xa = inp.x.astype(np.float64) @ a.astype(np.float64)
+    assert abs(l1 - l0) / abs(l0) <= TOL["f32"]["loss"]
+    assert np.abs((lse1 - lse0) - xa).max() <= TOL["f32"]["lse"] * max(1.0, np.abs(lse0).max())
+    assert norm_err(gx1, gx0) <= TOL["f32"]["grad"]
+    assert norm_err(gw1, gw0) <= TOL["f32"]["grad"]
+
+
 def test_targets_at_vocab_edges():
     inp = make_inputs("ragged", T=300, dtype="bf16", seed=3)
     inp.target[:] = np.where(np.arange(300) % 2 == 0, 0, 9999)
