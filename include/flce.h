@@ -207,8 +207,9 @@ int flce_timing_read(int64_t counts[FLCE_TIMING_ROLES], double ms[FLCE_TIMING_RO
  *   FLCE_TUNE_RASTER_ROWS  rows of a contraction's M dimension per raster group: tiles sweep
  *                          the N dimension inside a group, so the group's A rows stay in L2
  *                          while the B operand streams past. Multiple of 256; default 2048.
- *   FLCE_TUNE_SM_PAIRS     which bf16 contractions run on pairs of SMs (tcgen05 cta_group::2,
- *                          one MMA stream per pair) instead of single-SM 128 x 256 tiles: a bit
+ *   FLCE_TUNE_SM_PAIRS     which contractions run on pairs of SMs (tcgen05 cta_group::2,
+ *                          one MMA stream per pair) instead of single-SM 128 x 256 tiles, for
+ *                          bf16 and fp32 (3xTF32, 256 x 256 pair tiles) inputs alike: a bit
  *                          mask of FLCE_ROLE_FORWARD, FLCE_ROLE_DZ and FLCE_ROLE_GRADS; -1 (the default)
  *                          picks a measured mask when every SM of the current device can be
  *                          given a partner at once and 0 otherwise (how many pairs fit depends

@@ -599,8 +599,10 @@ int flce_forward(const void* x, const void* weight, const int64_t* target, int64
     for (int64_t v0 = 0; v0 < V && e == cudaSuccess; v0 += w.vf) {
       const int64_t sw = (V - v0) < w.vf ? (V - v0) : w.vf;
       CUtensorMap twh, twl;
-      if (!flce::make_tmap_2d(&twh, F, w.w_hi, H, sw, H * 4, 32, kTileN) ||
-          !flce::make_tmap_2d(&twl, F, w.w_lo, H, sw, H * 4, 32, kTileN))
+      const uint32_t wbox =
+          flce::core_b_box_rows(flce::tf32_core(dev.sms, FLCE_ROLE_FORWARD));
+      if (!flce::make_tmap_2d(&twh, F, w.w_hi, H, sw, H * 4, 32, wbox) ||
+          !flce::make_tmap_2d(&twl, F, w.w_lo, H, sw, H * 4, 32, wbox))
         return FLCE_ERR_CUDA;
       e = flce::launch_split_tf32(static_cast<const float*>(weight) + size_t(v0) * H, sw, H, H,
                                   w.w_hi, w.w_lo, false, s);
@@ -666,10 +668,12 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
         !flce::make_tmap_2d(&tx_mn, DT, x, H, T, H * 2, 64, 64))
       return FLCE_ERR_CUDA;
   } else {
+    // B operands boxed for their role's core (128 rows per CTA on SM pairs, 256 on one SM)
+    const uint32_t gbox = flce::core_b_box_rows(flce::tf32_core(dev.sms, FLCE_ROLE_GRADS));
     if (!flce::make_tmap_2d(&txh, DT, w.x_hi, H, T, H * 4, bk, kTileM) ||
         !flce::make_tmap_2d(&txl, DT, w.x_lo, H, T, H * 4, bk, kTileM) ||
-        !flce::make_tmap_2d(&txth, DT, w.xt_hi, T, H, w.ldT * 4, bk, kTileN) ||
-        !flce::make_tmap_2d(&txtl, DT, w.xt_lo, T, H, w.ldT * 4, bk, kTileN))
+        !flce::make_tmap_2d(&txth, DT, w.xt_hi, T, H, w.ldT * 4, bk, gbox) ||
+        !flce::make_tmap_2d(&txtl, DT, w.xt_lo, T, H, w.ldT * 4, bk, gbox))
       return FLCE_ERR_CUDA;
     const float* xf = static_cast<const float*>(x);
     e = flce::launch_split_tf32(xf, T, H, H, w.x_hi, w.x_lo, false, s);
@@ -749,14 +753,16 @@ int flce_backward(const void* x, const void* weight, const int64_t* target, cons
         e = flce::launch_split_tf32(wslab, sw, H, w.ldVc, w.wt_hi, w.wt_lo, true, s);
       if (e != cudaSuccess) break;
       CUtensorMap twh, twl, tdzth, tdztl, tdzh, tdzl, twth, twtl;
-      if (!flce::make_tmap_2d(&twh, DT, w.w_hi, H, sw, H * 4, bk, kTileN) ||
-          !flce::make_tmap_2d(&twl, DT, w.w_lo, H, sw, H * 4, bk, kTileN) ||
+      const uint32_t dbox = flce::core_b_box_rows(flce::tf32_core(dev.sms, FLCE_ROLE_DZ));
+      const uint32_t gbox = flce::core_b_box_rows(flce::tf32_core(dev.sms, FLCE_ROLE_GRADS));
+      if (!flce::make_tmap_2d(&twh, DT, w.w_hi, H, sw, H * 4, bk, dbox) ||
+          !flce::make_tmap_2d(&twl, DT, w.w_lo, H, sw, H * 4, bk, dbox) ||
           !flce::make_tmap_2d(&tdzth, DT, w.dzt_hi, T, sw, w.ldT * 4, bk, kTileM) ||
           !flce::make_tmap_2d(&tdztl, DT, w.dzt_lo, T, sw, w.ldT * 4, bk, kTileM) ||
           !flce::make_tmap_2d(&tdzh, DT, w.dz, sw, T, w.vc * 4, bk, kTileM) ||
           !flce::make_tmap_2d(&tdzl, DT, w.dz_lo, sw, T, w.vc * 4, bk, kTileM) ||
-          !flce::make_tmap_2d(&twth, DT, w.wt_hi, sw, H, w.ldVc * 4, bk, kTileN) ||
-          !flce::make_tmap_2d(&twtl, DT, w.wt_lo, sw, H, w.ldVc * 4, bk, kTileN))
+          !flce::make_tmap_2d(&twth, DT, w.wt_hi, sw, H, w.ldVc * 4, bk, gbox) ||
+          !flce::make_tmap_2d(&twtl, DT, w.wt_lo, sw, H, w.ldVc * 4, bk, gbox))
         return FLCE_ERR_CUDA;
       e = flce::timed_launch(1, s, [&] { return flce::launch_dz_tf32(txh, twh, txl, twl, dz); });
       if (e == cudaSuccess)

@@ -11,16 +11,22 @@
 
 namespace flce {
 
-// One problem M x N x K on the single-CTA core (operands K-major unless a_mn / b_mn).
+// One problem M x N x K with K-major operands: bf16 on the single-CTA core; fp32 (3xTF32, hi
+// and lo maps) on the core tf32_core(sms, role) picks, whose B maps are boxed for it.
 template <bool kTF32, class Epi>
 static cudaError_t run_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& ta_lo,
                             const CUtensorMap& tb_lo, int M, int N, int K, int* status, int sms,
                             cudaStream_t stream, const typename Epi::Args& ea,
-                            bool vocab_n = false) {
+                            bool vocab_n = false, int role = 0) {
+  const Core core = kTF32 ? tf32_core(sms, role) : kCoreSingle;
   GemmGrid g{};
-  g.p[0] = make_problem(M, N, K, StageGeom<kTF32>::kBK, false, false, kBM, 0, vocab_n);
+  g.p[0] = make_problem(M, N, K, StageGeom<kTF32>::kBK, false, false, core_tile_rows(core), 0,
+                        vocab_n);
   g.num_problems = 1;
   g.status = status;
+  if constexpr (kTF32) {
+    if (core == kCorePair) return launch_pair_tf32<Epi>(ta, tb, ta_lo, tb_lo, g, ea, sms, stream);
+  }
   return launch_gemm<kTF32, Epi, NoEpi>(ta, tb, ta_lo, tb_lo, g, ea, NoEpi::Args{}, sms, stream);
 }
 
@@ -56,7 +62,7 @@ cudaError_t launch_dz_tf32(const CUtensorMap& tx_hi, const CUtensorMap& tw_hi,
                                 p.slab0,
                                 p.slab_w};
   return run_gemm<true, DzEpi<true>>(tx_hi, tw_hi, tx_lo, tw_lo, p.T, p.slab_w, p.H, p.status,
-                                     p.sms, p.stream, ea, true);
+                                     p.sms, p.stream, ea, true, FLCE_ROLE_DZ);
 }
 
 // grad_W (A = dz slab, B = x, both MN-major, K = T) and grad_x (A = dz slab K-major, B = W slab
@@ -131,7 +137,7 @@ cudaError_t launch_gradw_tf32(const CUtensorMap& tdzt_hi, const CUtensorMap& txt
                               const GradWLaunch& p) {
   typename GradWEpi<true>::Args ea{p.grad_w, p.grad_loss, p.scale, p.H, p.slab0, p.slab_w};
   return run_gemm<true, GradWEpi<true>>(tdzt_hi, txt_hi, tdzt_lo, txt_lo, p.slab_w, p.H, p.T,
-                                        p.status, p.sms, p.stream, ea);
+                                        p.status, p.sms, p.stream, ea, false, FLCE_ROLE_GRADS);
 }
 
 cudaError_t launch_gradx_tf32(const CUtensorMap& tdz_hi, const CUtensorMap& twt_hi,
@@ -139,7 +145,7 @@ cudaError_t launch_gradx_tf32(const CUtensorMap& tdz_hi, const CUtensorMap& twt_
                               const GradXLaunch& p) {
   typename GradXEpi<true>::Args ea{p.acc, p.grad_x, p.grad_loss, p.scale, p.T, p.H, p.mode};
   return run_gemm<true, GradXEpi<true>>(tdz_hi, twt_hi, tdz_lo, twt_lo, p.T, p.H, p.K, p.status,
-                                        p.sms, p.stream, ea);
+                                        p.sms, p.stream, ea, false, FLCE_ROLE_GRADS);
 }
 
 // ---------------------------------------------------------------------------- TF32 split

@@ -117,12 +117,20 @@ template <bool kTF32>
 static cudaError_t launch_projection(const CUtensorMap& tx, const CUtensorMap& tw,
                                      const CUtensorMap& tx_lo, const CUtensorMap& tw_lo,
                                      const FwdLaunch& p, int col0, int cols) {
+  // bf16: single-SM tiles here (the pair cores launch from launch_forward_bf16); fp32: the
+  // core tf32_core picks, for which the W maps are boxed
+  const Core core = kTF32 ? tf32_core(p.sms, FLCE_ROLE_FORWARD) : kCoreSingle;
   GemmGrid g{};
-  g.p[0] = make_problem(p.T, cols, p.H, StageGeom<kTF32>::kBK, false, false, kBM, 0, true);
+  g.p[0] = make_problem(p.T, cols, p.H, StageGeom<kTF32>::kBK, false, false, core_tile_rows(core),
+                        0, true);
   g.num_problems = 1;
   g.status = p.status;
   g.tile_counter = p.tile_counter;
   FwdEpi::Args ea{p.target, p.part_m, p.part_s, p.zy, p.sx, p.T, cols, col0};
+  if constexpr (kTF32) {
+    if (core == kCorePair)
+      return launch_pair_tf32<FwdEpi>(tx, tw, tx_lo, tw_lo, g, ea, p.sms, p.stream);
+  }
   return launch_gemm<kTF32, FwdEpi, NoEpi>(tx, tw, tx_lo, tw_lo, g, ea, NoEpi::Args{}, p.sms,
                                            p.stream);
 }

@@ -88,6 +88,11 @@ inline Core role_core(int sms, int role) {
   const int w = tune_wide_tiles();
   return ((w >= 0 ? w : kDefaultWideRoles) & role) ? kCoreWide : kCorePair;
 }
+// The contraction core an fp32 (3xTF32) role launches on: CTA pairs with 128-row CTA tiles
+// (256 x 256 pair tiles) when the role runs on SM pairs, else single-SM 128 x 256 tiles.
+inline Core tf32_core(int sms, int role) {
+  return (pair_roles(sms) & role) != 0 ? kCorePair : kCoreSingle;
+}
 // M rows of one tile (GemmProblem tile_rows) on a core.
 inline int core_tile_rows(Core c) { return c == kCoreWide ? 512 : c == kCorePair ? 256 : 128; }
 // Rows of the box of a K-major A operand map ({64 x rows}) on a core.

@@ -1,4 +1,5 @@
-// gemm_pair.cuh - the bf16 contraction core on CTA pairs (tcgen05 cta_group::2).
+// gemm_pair.cuh - the contraction core on CTA pairs (tcgen05 cta_group::2): bf16 operands, or
+// fp32 operands as 3xTF32 (hi, lo) copies on 128-row CTA tiles (kTF32x3, see PairGeom).
 //
 // A cluster of two CTAs on two SMs computes one (2 kRows) x 256 output tile with one MMA stream:
 // CTA r holds rows [kRows r, kRows r + kRows) of the A tile and rows [128r, 128r + 128) of the
@@ -45,17 +46,24 @@ namespace flce {
 // kSplit: epilogue warps per (lane quarter, 128-row half): 1 drains all 256 columns of its
 // rows, 2 gives each of two warps 128 of them (16 epilogue warps on wide tiles), which halves
 // the time a finished tile keeps the single accumulator of the wide geometry busy.
-template <int kRows, int kSplit = 1>
+// kTF32x3: fp32 operands as TF32 (hi, lo) copies (3xTF32, 128-row CTA tiles only): a stage
+// holds [A_hi][A_lo][B_hi][B_lo], each a 128-byte row of 32 fp32 per operand row, and the
+// 512 TMEM columns hold one tile's two accumulators, hi.hi at column 0 and the corrections
+// hi.lo + lo.hi at column 256 (kept apart so that the small terms are not truncated against
+// the large ones), summed in fp32 by the epilogue.
+template <int kRows, int kSplit = 1, bool kTF32x3 = false>
 struct PairGeom {
   static_assert(kRows == 128 || kRows == 256, "rows per CTA: 128 or 256");
   static_assert(kSplit == 1 || kSplit == 2, "epilogue warps per row block: 1 or 2");
+  static_assert(!kTF32x3 || (kRows == 128 && kSplit == 1), "3xTF32: 128-row CTA tiles");
   static constexpr int kHalves = kRows / 128;          // M=256 MMAs per K step / epilogue halves
-  static constexpr int kStages = kRows == 128 ? 6 : 4;
-  static constexpr uint32_t kABytes = kRows * 128;     // kRows rows x 64 bf16
-  static constexpr uint32_t kBBytes = 128 * 128;       // this CTA's 128 N rows x 64 bf16
-  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr int kCopies = kTF32x3 ? 2 : 1;      // hi (+ lo) copy of each operand
+  static constexpr int kStages = kTF32x3 ? 3 : (kRows == 128 ? 6 : 4);
+  static constexpr uint32_t kABytes = kRows * 128;     // kRows rows x 128 B (64 bf16 / 32 fp32)
+  static constexpr uint32_t kBBytes = 128 * 128;       // this CTA's 128 N rows x 128 B
+  static constexpr uint32_t kStageBytes = kCopies * (kABytes + kBBytes);
   static constexpr uint32_t kRingBytes = kStages * kStageBytes;
-  static constexpr int kAccBufs = 2 / kHalves;         // accumulators in the 512 TMEM columns
+  static constexpr int kAccBufs = kTF32x3 ? 1 : 2 / kHalves;  // tiles in the 512 TMEM columns
   static constexpr int kEpiWarps = 4 * kHalves * kSplit;
   // ring, barrier/slot block (1 KB), store staging per epilogue warp, alignment slack
   static constexpr uint32_t kSmemBytes = kRingBytes + 1024 + kEpiWarps * kEpiStageBytes + 1024;
@@ -67,16 +75,18 @@ constexpr int kPairBK = 64;
 
 // GemmProblem::m_tiles counts pair tiles of 2 kRows rows (make_problem with tile_rows =
 // PairGeom<kRows>::kTileRows) and the epilogue receives 128-row block indices.
-template <int kRows, int kSplit, class Epi0, class Epi1>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSplit>::kThreads, 1)
+template <int kRows, int kSplit, class Epi0, class Epi1, bool kTF32x3 = false>
+__global__ void __cluster_dims__(2, 1, 1)
+    __launch_bounds__(PairGeom<kRows, kSplit, kTF32x3>::kThreads, 1)
     k_umma_gemm_pair(const __grid_constant__ CUtensorMap tA0,
                      const __grid_constant__ CUtensorMap tB0,
                      const __grid_constant__ CUtensorMap tA1,
                      const __grid_constant__ CUtensorMap tB1, const GemmGrid g,
                      const typename Epi0::Args e0, const typename Epi1::Args e1) {
-  using G = PairGeom<kRows, kSplit>;
+  using G = PairGeom<kRows, kSplit, kTF32x3>;
   // wide tiles with one warp per (lane quarter, column half) may drain their halves in order
   constexpr bool kOrderable = G::kHalves == 2 && kSplit == 1;
+  constexpr int kBK = kTF32x3 ? 32 : kPairBK;  // K elements per stage (one 128-byte row)
   constexpr int kPairStages = G::kStages;
   constexpr uint32_t kPairABytes = G::kABytes;
   constexpr uint32_t kPairStageBytes = G::kStageBytes;
@@ -196,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
         const CUtensorMap* tb = pt.prob ? &tB1 : &tB0;
         const int m0 = pt.mb * G::kTileRows + static_cast<int>(rank) * kRows;
         const int n0 = pt.nb * 256 + static_cast<int>(rank) * 128;
-        const bool a_mn = pt.a_mn != 0, b_mn = pt.b_mn != 0;
+        const bool a_mn = !kTF32x3 && pt.a_mn != 0, b_mn = !kTF32x3 && pt.b_mn != 0;
         const int k_blocks = pt.k_blocks;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, g.status, abort_flag)) {
@@ -206,20 +216,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
           if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * kPairStageBytes);
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           const uint32_t sA = ring + stage * kPairStageBytes;
-          const uint32_t sB = sA + kPairABytes;
-          const int k0 = kb * kPairBK;
-          if (!a_mn) {  // one box of kRows rows (the A map is boxed {64 x kRows})
+          const uint32_t sB = sA + G::kCopies * kPairABytes;
+          const int k0 = kb * kBK;
+          if constexpr (kTF32x3) {  // K-major hi and lo copies: tA0/tB0 hi, tA1/tB1 lo
+            tma_load_2d_pair(sA, &tA0, fb, k0, m0);
+            tma_load_2d_pair(sA + kPairABytes, &tA1, fb, k0, m0);
+            tma_load_2d_pair(sB, &tB0, fb, k0, n0);
+            tma_load_2d_pair(sB + G::kBBytes, &tB1, fb, k0, n0);
+          } else if (!a_mn) {  // one box of kRows rows (the A map is boxed {64 x kRows})
             tma_load_2d_pair(sA, ta, fb, k0, m0);
           } else {  // kRows / 64 boxes of {64 (M) x 64 (K)}
 #pragma unroll
             for (int j = 0; j < kRows / 64; ++j)
               tma_load_2d_pair(sA + 8192u * j, ta, fb, m0 + 64 * j, k0);
           }
-          if (!b_mn) {
-            tma_load_2d_pair(sB, tb, fb, k0, n0);
-          } else {
-            tma_load_2d_pair(sB, tb, fb, n0, k0);
-            tma_load_2d_pair(sB + 8192u, tb, fb, n0 + 64, k0);
+          if constexpr (!kTF32x3) {
+            if (!b_mn) {
+              tma_load_2d_pair(sB, tb, fb, k0, n0);
+            } else {
+              tma_load_2d_pair(sB, tb, fb, n0, k0);
+              tma_load_2d_pair(sB + 8192u, tb, fb, n0 + 64, k0);
+            }
           }
           ++fills;
           if (++stage == kPairStages) {
@@ -252,15 +269,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
         }
         if (t < 0) break;
         const TileInfo pt = map_tile(g, t);
-        const bool a_mn = pt.a_mn != 0, b_mn = pt.b_mn != 0;
+        const bool a_mn = !kTF32x3 && pt.a_mn != 0, b_mn = !kTF32x3 && pt.b_mn != 0;
         const int k_blocks = pt.k_blocks;
-        const uint32_t idesc = idesc_f32acc(kFmtBF16, 256, 256, a_mn, b_mn);
+        const uint32_t idesc =
+            idesc_f32acc(kTF32x3 ? kFmtTF32 : kFmtBF16, 256, 256, a_mn, b_mn);
         // Descriptor of stage 0 and the per-K-step advance (in 16-byte units): K-major moves
         // 32 B along the swizzled row, MN-major moves 16 K rows of 128 B.
         const uint64_t a_base =
             a_mn ? sdesc_sw128(ring, 8192u, 1024u) : sdesc_sw128(ring, 16u, 1024u);
-        const uint64_t b_base = b_mn ? sdesc_sw128(ring + kPairABytes, 8192u, 1024u)
-                                     : sdesc_sw128(ring + kPairABytes, 16u, 1024u);
+        const uint32_t sB0 = ring + G::kCopies * kPairABytes;
+        const uint64_t b_base = b_mn ? sdesc_sw128(sB0, 8192u, 1024u) : sdesc_sw128(sB0, 16u, 1024u);
         const uint64_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
         const uint64_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
         // Accumulator handshake with both CTAs' epilogues: cluster-scope acquire.
@@ -328,11 +346,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
             const uint64_t soff = static_cast<uint64_t>(stage * kPairStageBytes) >> 4;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+              if constexpr (kTF32x3) {
+                // corrections lo.hi + hi.lo into their own accumulator, then hi.hi
+                const uint64_t a_hi = a_base + soff + kk * a_step;
+                const uint64_t b_hi = b_base + soff + kk * b_step;
+                const uint64_t a_lo = a_hi + (kPairABytes >> 4);
+                const uint64_t b_lo = b_hi + (G::kBBytes >> 4);
+                const uint32_t d_corr = d_tmem + static_cast<uint32_t>(kBN);
+                mma_tf32_pair(d_corr, a_lo, b_hi, idesc, accum);
+                mma_tf32_pair(d_corr, a_hi, b_lo, idesc, 1u);
+                mma_tf32_pair(d_tmem, a_hi, b_hi, idesc, accum);
+              } else {
 #pragma unroll
-              for (int h = 0; h < G::kHalves; ++h)
-                mma_bf16_pair(d_tmem + static_cast<uint32_t>(h * kBN),
-                              a_base + soff + h * (16384u >> 4) + kk * a_step,
-                              b_base + soff + kk * b_step, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                for (int h = 0; h < G::kHalves; ++h)
+                  mma_bf16_pair(d_tmem + static_cast<uint32_t>(h * kBN),
+                                a_base + soff + h * (16384u >> 4) + kk * a_step,
+                                b_base + soff + kk * b_step, idesc, accum);
+              }
             }
             mma_commit_pair(empty_bar(stage), 0x3);
             ++consumed;
@@ -434,8 +465,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
         ctx.c_end = ctx.c_begin + kBN / 32 / ctx.split;
         ctx.part = col_part;
         ctx.iter = iter;
-        ctx.two_acc = 0;
-        ctx.taddr_corr = 0;
+        ctx.two_acc = kTF32x3 ? 1 : 0;
+        ctx.taddr_corr = ctx.taddr + static_cast<uint32_t>(kBN);  // 3xTF32: the corrections
         ctx.xbar = x_bar(quarter + 4 * h);
         ctx.xchg = ordered ? xchg_ordered + 64 * h : xchg;
         ctx.status = g.status;
@@ -493,9 +524,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairGeom<kRows, kSpl
 
 // How many CTA pairs of `kern` can be resident at once on the current device (queried once
 // per device and kernel). Depends on how the chip's SMs are grouped, not only on their count.
-template <int kRows, int kSplit, class K>
+template <int kRows, int kSplit, bool kTF32x3 = false, class K>
 int pair_resident_clusters(K kern, int sms) {
-  using G = PairGeom<kRows, kSplit>;
+  using G = PairGeom<kRows, kSplit, kTF32x3>;
   static int cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return sms / 2;
@@ -516,16 +547,16 @@ int pair_resident_clusters(K kern, int sms) {
 // Launch one or two problems on CTA pairs: a persistent grid of as many pairs as can be
 // resident at once (at most one per tile). The problems' m_tiles count PairGeom<kRows>::
 // kTileRows-row tiles, and K-major A operands are boxed {64 x kRows}.
-template <int kRows, int kSplit, class Epi0, class Epi1>
+template <int kRows, int kSplit, class Epi0, class Epi1, bool kTF32x3 = false>
 cudaError_t launch_pair(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
                         const CUtensorMap& b1, GemmGrid g, const typename Epi0::Args& e0,
                         const typename Epi1::Args& e1, int sms, cudaStream_t stream) {
-  using G = PairGeom<kRows, kSplit>;
-  auto kern = k_umma_gemm_pair<kRows, kSplit, Epi0, Epi1>;
+  using G = PairGeom<kRows, kSplit, kTF32x3>;
+  auto kern = k_umma_gemm_pair<kRows, kSplit, Epi0, Epi1, kTF32x3>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmemBytes);
   if (e != cudaSuccess) return e;
-  const int max_clusters = pair_resident_clusters<kRows, kSplit>(kern, sms);
+  const int max_clusters = pair_resident_clusters<kRows, kSplit, kTF32x3>(kern, sms);
   finish_grid(g);
   if (g.tile_counter) {
     e = cudaMemsetAsync(g.tile_counter, 0, sizeof(int), stream);
@@ -555,6 +586,19 @@ cudaError_t launch_pair_core(Core core, const CUtensorMap& a0, const CUtensorMap
     return launch_pair<256, 1, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
   }
   return launch_pair<128, 1, Epi0, Epi1>(a0, b0, a1, b1, g, e0, e1, sms, stream);
+}
+
+// fp32 (3xTF32) problem on CTA pairs with 128-row CTA tiles (256 x 256 pair tiles): every
+// operand K-major, a_hi / b_hi the TF32 hi copies and a_lo / b_lo the lo copies; A maps boxed
+// {32 x 128}, B maps {32 x 128} (one CTA's N half); the problem made with 256-row tiles and
+// 32-deep K blocks.
+template <class Epi>
+cudaError_t launch_pair_tf32(const CUtensorMap& a_hi, const CUtensorMap& b_hi,
+                             const CUtensorMap& a_lo, const CUtensorMap& b_lo, GemmGrid g,
+                             const typename Epi::Args& e, int sms, cudaStream_t stream) {
+  g.ordered = 0;
+  return launch_pair<128, 1, Epi, NoEpi, true>(a_hi, b_hi, a_lo, b_lo, g, e, NoEpi::Args{}, sms,
+                                               stream);
 }
 
 }  // namespace flce

@@ -202,6 +202,27 @@ def test_contraction_cores_agree():
             assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("shape", [(300, 264, 700), (1269, 1000, 10000)])
+def test_fp32_single_sm_and_sm_pair_tiles(shape):
+    """The fp32 (3xTF32) contractions on single-SM 128 x 256 tiles and on SM pairs with 128-row
+    CTA tiles: both within the fp32 tolerances of the oracle, and equal bit for bit (the same
+    three products per K step, summed in the same order into the same two accumulators)."""
+    T, H, V = shape
+    inp = make_inputs("tiny", T=T, H=H, V=V, dtype="f32", seed=43)
+    runs = []
+    try:
+        for pair in (0, 7):
+            B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
+            assert B.flce_get_tuning(B.FLCE_TUNE_SM_PAIRS) == pair
+            runs.append(assert_full_parity(inp, "mean", grad_loss=1.5,
+                                           label=f"fp32 {T}x{H}x{V} pair={pair}"))
+    finally:
+        B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, -1)
+    assert runs[0][0] == runs[1][0]
+    for a, b in zip(runs[0][1:], runs[1][1:]):
+        assert np.array_equal(a, b)
+
+
 def test_drain_modes_agree_with_many_tiles_per_pair():
     """Wide pair tiles drained half by half (the next tile's MMAs on the first half start while
     the second half is read) or both halves together, or by 16 epilogue warps, give the same
