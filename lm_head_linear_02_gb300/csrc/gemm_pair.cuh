@@ -155,7 +155,7 @@ __global__ void __cluster_dims__(2, 1, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch(&tA0);
     tma_prefetch(&tB0);
-    if (g.num_problems > 1) {
+    if (kTF32x3 || g.num_problems > 1) {  // the second problem's maps, or the lo copies' maps
       tma_prefetch(&tA1);
       tma_prefetch(&tB1);
     }
@@ -278,7 +278,8 @@ __global__ void __cluster_dims__(2, 1, 1)
         const uint64_t a_base =
             a_mn ? sdesc_sw128(ring, 8192u, 1024u) : sdesc_sw128(ring, 16u, 1024u);
         const uint32_t sB0 = ring + G::kCopies * kPairABytes;
-        const uint64_t b_base = b_mn ? sdesc_sw128(sB0, 8192u, 1024u) : sdesc_sw128(sB0, 16u, 1024u);
+        const uint64_t b_base =
+            b_mn ? sdesc_sw128(sB0, 8192u, 1024u) : sdesc_sw128(sB0, 16u, 1024u);
         const uint64_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
         const uint64_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
         // Accumulator handshake with both CTAs' epilogues: cluster-scope acquire.
