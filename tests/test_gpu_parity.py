@@ -390,16 +390,18 @@ def test_out_of_range_target_sets_status_and_nan_loss():
         A.check_status(status)
 
 
-@pytest.mark.parametrize("pair,wide,split,ordered", [(0, 0, -1, 0), (7, 0, -1, 0), (7, 7, -1, 0),
-                                                     (7, 7, 3, 0), (7, 7, -1, 7)])
-def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide, split, ordered):
+@pytest.mark.parametrize("pair,wide,split,ordered,dtype", [
+    (0, 0, -1, 0, "bf16"), (7, 0, -1, 0, "bf16"), (7, 7, -1, 0, "bf16"), (7, 7, 3, 0, "bf16"),
+    (7, 7, -1, 7, "bf16"), (0, 0, -1, 0, "f32"), (7, 0, -1, 0, "f32")])
+def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide, split, ordered, dtype):
     """A withheld pipeline signal ends the launch with FLCE_STATUS_TIMEOUT after the bounded wait
     (about 2 s) instead of hanging, on each contraction core (single SM, SM pairs with 128-row
     and with 256-row CTA tiles, whose abort path also drains the partner CTA, and the latter
-    with its row halves drained in order); the next calls run normally on the same context."""
+    with its row halves drained in order; fp32 on single-SM and on pair tiles); the next calls
+    run normally on the same context."""
     import time
 
-    inp = make_inputs("ragged", dtype="bf16")
+    inp = make_inputs("ragged", dtype=dtype)
     x, w, y = to_device(inp)
     B.flce_set_tuning(B.FLCE_TUNE_SM_PAIRS, pair)
     B.flce_set_tuning(B.FLCE_TUNE_WIDE_TILES, wide)
@@ -421,7 +423,7 @@ def test_pipeline_timeout_is_reported_and_device_stays_usable(pair, wide, split,
         B.flce_set_tuning(B.FLCE_TUNE_SPLIT_EPILOGUE, -1)
         B.flce_set_tuning(B.FLCE_TUNE_ORDERED_DRAIN, -1)
     assert_full_parity(inp, "mean", label=f"after timeout pair={pair} wide={wide} split={split} "
-                       f"ordered={ordered}")
+                       f"ordered={ordered} {dtype}")
 
 
 def test_sum_mean_and_grad_loss_scaling():
