@@ -70,7 +70,8 @@ constexpr int kDefaultSplitEpilogue = 0;
 // and dz, whose K = H main loops are short enough for the drain to matter. Measured on GB300
 // at T = 16384, H = 4096, V = 128256 against draining both halves together: a tile's period
 // (SM clock stamps per tile) 1.4% shorter for the forward and 2.3% for dz; in the power-capped
-// step the forward launch 0.6% and dz 1.4% faster, the step 0.3-0.5%. The gradient launch
+// step the forward launch 0.6% and dz 1.4% faster, the step 0.3-0.5%; the single call's chunk
+// logits (forward role) 1.4% faster (three interleaved runs each). The gradient launch
 // (K = 16384 or 32256) loses: its epilogue's accumulator traffic during the next tile's main
 // loop made its tiles 3% longer.
 constexpr int kDefaultOrderedDrain = FLCE_ROLE_FORWARD | FLCE_ROLE_DZ;
