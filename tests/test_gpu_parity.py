@@ -317,6 +317,44 @@ def test_shift_of_all_weight_rows_f32():
     assert norm_err(gw1, gw0) <= TOL["f32"]["grad"]
 
 
+def _random_shapes(n, seed):
+    """Seeded ragged shapes: T in [1, 1500], H a multiple of 8 in [8, 1024], V in [2, 6000]."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        T = int(rng.integers(1, 1501))
+        H = 8 * int(rng.integers(1, 129))
+        V = int(rng.integers(2, 6001))
+        dtype = "bf16" if i % 2 == 0 else "f32"
+        reduction = ("mean", "sum", "none")[i % 3]
+        out.append((T, H, V, dtype, reduction))
+    return out
+
+
+@pytest.mark.parametrize("T,H,V,dtype,reduction", _random_shapes(8, 2026))
+def test_parity_random_ragged_shapes(T, H, V, dtype, reduction):
+    """Ragged shapes drawn at random (every dimension off the tile grid in most draws) on the
+    default cores, element by element against the oracle at the dtype's tolerances; 'none'
+    with a random per-token upstream gradient."""
+    inp = make_inputs("tiny", T=T, H=H, V=V, dtype=dtype, seed=T + H + V)
+    if reduction != "none":
+        assert_full_parity(inp, reduction, grad_loss=0.5, label=f"{T}x{H}x{V} {dtype} {reduction}")
+        return
+    u = np.random.default_rng(V).standard_normal(T).astype(np.float32)
+    x, w, y = to_device(inp)
+    loss, lse, status = A.flce_forward(x, w, y, "none")
+    gx, gw, status = A.flce_backward(x, w, y, lse, torch.from_numpy(u).cuda(), "none",
+                                     status=status)
+    torch.cuda.synchronize()
+    A.check_status(status)
+    ref = oracle.flce(inp.x, inp.weight, inp.target, "none", grad_loss=u.astype(np.float64))
+    tol = TOL[dtype]
+    per = loss.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(per - ref["loss"]) / np.abs(ref["loss"])) <= tol["loss"]
+    assert norm_err(gx.float().cpu().numpy().astype(np.float64), ref["grad_x"]) <= tol["grad"]
+    assert norm_err(gw.float().cpu().numpy().astype(np.float64), ref["grad_weight"]) <= tol["grad"]
+
+
 def test_targets_at_vocab_edges():
     inp = make_inputs("ragged", T=300, dtype="bf16", seed=3)
     inp.target[:] = np.where(np.arange(300) % 2 == 0, 0, 9999)
