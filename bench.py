@@ -201,9 +201,17 @@ class ClockSampler:
                 continue
             try:
                 ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                rows.append((ts, float(r[1]), float(r[2]), r[5:9]))
             except ValueError:
                 continue
+            try:
+                sm, sm_max = float(r[1]), float(r[2])
+            except ValueError:
+                continue
+            try:
+                power = float(r[3])
+            except ValueError:  # "[N/A]" on boards that do not report it
+                power = float("nan")
+            rows.append((ts, sm, sm_max, r[5:9], power))
         inside = [r for r in rows
                   if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
         use = inside or rows
@@ -211,8 +219,10 @@ class ClockSampler:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = {n for r in use for n, v in zip(names, r[3]) if v.lower() == "active"}
+        powers = [r[4] for r in use if r[4] == r[4]]
         return {"sm_mhz": statistics.median(r[1] for r in use),
                 "sm_max_mhz": max(r[2] for r in use), "reasons": sorted(reasons),
+                "power_w": statistics.median(powers) if powers else None,
                 "samples": len(use), "in_timed_window": bool(inside)}
 
 

@@ -88,3 +88,44 @@ def test_tuning_arguments_parse_and_refuse_unknown_names():
     for bad in (["raster_vocab"], ["nonsense=1"], ["raster_vocab=abc"]):
         with pytest.raises(ValueError):
             bench.parse_tuning(bad)
+
+
+def test_clock_sampler_keeps_the_timed_window_and_reports_power():
+    """The nvidia-smi sampler keeps the rows stamped inside the timed window: median SM clock,
+    maximum clock, the throttle reasons seen active, and the median board power (rows whose
+    power reads "[N/A]" are left out of that median)."""
+    import datetime
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    def stamp(sec):
+        return datetime.datetime.fromtimestamp(sec).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+
+    t0 = 1_800_000_000.0
+    rows = [
+        (t0 - 1.0, 2070, 400.0, "Not Active"),  # before the window
+        (t0 + 0.1, 1600, 1390.0, "Active"),
+        (t0 + 0.2, 1620, 1380.0, "Active"),
+        (t0 + 0.3, 1640, None, "Active"),
+        (t0 + 5.0, 2070, 300.0, "Not Active"),  # after the window
+    ]
+    text = "\n".join(
+        f"{stamp(ts)}, {sm}, 2070, {'[N/A]' if pw is None else pw}, 0x4, Not Active, Not Active, "
+        f"Not Active, {cap}" for ts, sm, pw, cap in rows)
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def communicate(self, timeout=None):
+            return text, ""
+
+    s = bench.ClockSampler(0)
+    s.proc = FakeProc()
+    s.t0, s.t1 = t0, t0 + 1.0
+    out = s.stop()
+    assert out["in_timed_window"] and out["samples"] == 3
+    assert out["sm_mhz"] == 1620 and out["sm_max_mhz"] == 2070
+    assert out["reasons"] == ["sw_power_cap"]
+    assert out["power_w"] == pytest.approx(1385.0)
