@@ -159,7 +159,8 @@ class ClockSampler:
     """nvidia-smi clock/throttle sampling during the timed region: samples every 100 ms,
     timestamped, of which those inside the window marked by begin()/end() are kept."""
 
-    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    # power.draw.instant: power.draw is a one-second average, longer than a short timed region
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw.instant,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
